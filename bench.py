@@ -1,0 +1,524 @@
+#!/usr/bin/env python
+"""Benchmark: one displaced denoising step of the whole hot path per step.
+
+A step runs, through the C ABI, on the SDXL-3840px-with-guidance workload
+(latent 480x480, batch 2 = conditional + unconditional, 8 bands):
+  1. displaced 3x3 conv 320->320 on [2,480,480,320]        (dpp_conv3x3)
+  2. displaced GroupNorm (32 groups) on the conv output     (dpp_groupnorm)
+  3. displaced self-attention, 2 x 57600 tokens, C=640,
+     10 heads of 64: QKV projection writing the fresh K/V
+     state, attention core, output projection             (dpp_self_attn)
+  4. cross-attention of the result over 77 x 2048 text
+     context tokens                                        (dpp_cross_attn)
+  5. guidance combine + rel-MAE sums, 2 x [4,480,480] fp32 (dpp_cfg_combine)
+  6. refresh of the conv's stale buffer with this step's
+     input (the all_gather)                                (dpp_refresh_stale)
+The GroupNorm statistics and attention K/V states ping-pong between two
+buffers, as consecutive denoising steps do.
+
+Printed metric: tensor TFLOP/s of the step (conv + self-attention core and
+projections + cross-attention; the bandwidth ops add time but no FLOPs),
+with per-op numbers and roofline fractions alongside.  Inputs and the step's
+working set (~2.5 GB) exceed the 126 MB L2, so no explicit flush is done.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "displaced-patch conv/attn TFLOP/s, GroupNorm GB/s; % of B300 roofline"
+WORKLOAD = "sdxl_3840_cfg"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ------------------------------------------------------------------ work model
+def work_model(w):
+    """Algorithmic FLOPs / bytes per step (counting rules of the method's ops:
+    tensor-core MMAs only; GroupNorm = read x + write y; refresh = read +
+    write the band; guidance = read u, c + write out)."""
+    c, a = w.conv, w.attn
+    conv = 2.0 * c.B * c.H * c.W * c.C * 9 * c.C
+    core = 4.0 * a.B * a.N * a.N * a.head_dim * a.heads
+    proj = 2.0 * a.B * a.N * a.C * 3 * a.C + 2.0 * a.B * a.N * a.C * a.C
+    xq_o = 2.0 * 2.0 * a.B * a.N * a.C * a.C
+    xkv = 2.0 * a.B * a.n_ctx * a.c_ctx * 2 * a.C
+    xcore = 4.0 * a.B * a.N * a.n_ctx * a.head_dim * a.heads
+    act_bytes = c.B * c.H * c.W * c.C * 2
+    n_cfg = int(np.prod(w.cfg_shape))
+    return {
+        "conv_flop": conv, "self_core_flop": core, "self_proj_flop": proj,
+        "cross_flop": xq_o + xkv + xcore, "cross_core_flop": xcore,
+        "gn_bytes": 2.0 * act_bytes, "refresh_bytes": 2.0 * act_bytes,
+        "cfg_bytes": 3.0 * 4 * n_cfg,
+        "step_flop": conv + core + proj + xq_o + xkv + xcore,
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.dev = self._gpu_id(device_index)
+        self.proc = None
+        self.lines = []
+
+    @staticmethod
+    def _gpu_id(idx):
+        try:
+            u = str(torch.cuda.get_device_properties(idx).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            return vis.split(",")[idx] if vis else str(idx)
+
+    def start(self):
+        cmd = ["nvidia-smi", "-i", self.dev, "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our step
+class Step:
+    """Device buffers and one displaced step of the hot path through the C ABI."""
+
+    def __init__(self, w, dev):
+        import displaced_patch_parallelism_02_b300 as dpp
+        self.dpp = dpp
+        self.w = w
+        c, a = w.conv, w.attn
+        bf = torch.bfloat16
+        self.stream = torch.cuda.current_stream(dev)
+        put = lambda t: t.contiguous().to(dev)
+        shape = (c.B, c.H, c.W, c.C)
+        F = wl.normal(shape, wl.seed_of(w.index, 0, wl.T_FRESH), dtype=w.dtype)
+        S = wl.perturbed(F, wl.seed_of(w.index, 1, wl.T_STALE_NOISE), w.stale_scale)
+        self.host_x = F.pin_memory()
+        self.x, self.stale = put(F), put(S)
+        del F, S
+        self.wconv = put(wl.conv_weight(c.C, c.C, wl.seed_of(w.index, 0, wl.T_CONV_W),
+                                        w.dtype).permute(0, 2, 3, 1))
+        self.y1 = torch.empty(shape, dtype=bf, device=dev)
+        self.y2 = torch.empty(shape, dtype=bf, device=dev)
+        g, b = wl.gn_affine(c.C, w.index)
+        self.gamma, self.beta = put(g), put(b)
+        self.gn_desc = dpp.dpp_gn_desc(c.B, c.H, c.W, c.C, w.groups, c.P, w.eps, dpp.DPP_BF16)
+        self.gn_ws_n = dpp.dpp_groupnorm_workspace_bytes(self.gn_desc)
+        self.gn_ws = torch.empty(self.gn_ws_n, dtype=torch.uint8, device=dev)
+        self.stats = [torch.empty((c.P, c.B, w.groups, 2), device=dev) for _ in range(2)]
+        self.conv_desc = dpp.dpp_conv_desc(c.B, c.H, c.W, c.C, c.C, c.P, dpp.DPP_BF16, 0)
+        # attention level
+        X = wl.normal((a.B, a.N, a.C), wl.seed_of(w.index, 0, wl.T_ATTN_X), dtype=w.dtype)
+        Xs = wl.perturbed(X, wl.seed_of(w.index, 1, wl.T_ATTN_X), w.stale_scale)
+        self.host_xa = X.pin_memory()
+        self.xa = put(X)
+        xs = put(Xs)
+        del X, Xs
+        self.aw = {k: put(v) for k, v in wl.attn_weights(a, w.index, w.dtype).items()}
+        self.xw = {k: put(v) for k, v in wl.cross_weights(a, w.index, w.dtype).items()}
+        ctx = wl.context(a, w.index, w.dtype)
+        self.host_ctx = ctx.pin_memory()
+        self.ctx = put(ctx)
+        self.attn_desc = dpp.dpp_attn_desc(a.B, a.H, a.W, a.C, a.heads, a.head_dim, a.P, 0, 0,
+                                           dpp.DPP_BF16)
+        self.cross_desc = dpp.dpp_attn_desc(a.B, a.H, a.W, a.C, a.heads, a.head_dim, 1,
+                                            a.n_ctx, a.c_ctx, dpp.DPP_BF16)
+        self.sa_ws_n = dpp.dpp_self_attn_workspace_bytes(self.attn_desc)
+        self.sa_ws = torch.empty(self.sa_ws_n, dtype=torch.uint8, device=dev)
+        self.xa_ws_n = dpp.dpp_cross_attn_workspace_bytes(self.cross_desc)
+        self.xa_ws = torch.empty(self.xa_ws_n, dtype=torch.uint8, device=dev)
+        self.kv = [torch.empty((a.B, a.N, 2, a.C), dtype=bf, device=dev) for _ in range(2)]
+        self.ya = torch.empty((a.B, a.N, a.C), dtype=bf, device=dev)
+        self.yc = torch.empty((a.B, a.N, a.C), dtype=bf, device=dev)
+        # guidance maps
+        u, cc = wl.guidance_maps(w.cfg_shape, w.index)
+        self.host_u, self.host_c = u.pin_memory(), cc.pin_memory()
+        self.u, self.c = put(u), put(cc)
+        self.n_cfg = u.numel()
+        self.cfg_out = torch.empty_like(self.u)
+        self.sums = torch.zeros(3, dtype=torch.float64, device=dev)
+        self.cfg_ws_n = dpp.dpp_cfg_workspace_bytes(self.n_cfg)
+        self.cfg_ws = torch.zeros(self.cfg_ws_n, dtype=torch.uint8, device=dev)
+        # step "t-1": synchronous calls on the stale inputs seed the states
+        s = self.stream
+        dpp.dpp_conv3x3(self.conv_desc, self.stale, None, self.wconv, None, self.y1, stream=s)
+        dpp.dpp_groupnorm(self.gn_desc, self.y1, None, self.stats[0], self.gamma, self.beta,
+                          self.y2, self.gn_ws, self.gn_ws_n, stream=s)
+        dpp.dpp_self_attn(self.attn_desc, xs, self.aw["wq"], self.aw["wk"], self.aw["wv"],
+                          self.aw["wo"], None, self.kv[0], self.ya, self.sa_ws, self.sa_ws_n,
+                          stream=s)
+        torch.cuda.synchronize(dev)
+        del xs
+        self.i = 0
+        c_ = w.conv
+        self.row_bytes = c_.W * c_.C * 2
+        self.ops = ["conv", "groupnorm", "self_attn", "cross_attn", "cfg", "refresh"]
+
+    def run(self, events=None, core_events=None):
+        """One displaced step; events (len 7) bracket the six ABI calls."""
+        dpp, s, w = self.dpp, self.stream, self.w
+        c = w.conv
+        k0, k1 = self.i % 2, (self.i + 1) % 2
+        rec = (lambda j: events[j].record(s)) if events else (lambda j: None)
+        rec(0)
+        dpp.dpp_conv3x3(self.conv_desc, self.x, self.stale, self.wconv, None, self.y1, stream=s)
+        rec(1)
+        dpp.dpp_groupnorm(self.gn_desc, self.y1, self.stats[k0], self.stats[k1], self.gamma,
+                          self.beta, self.y2, self.gn_ws, self.gn_ws_n, stream=s)
+        rec(2)
+        if core_events:
+            dpp.dpp_set_attn_core_events(*core_events)
+        dpp.dpp_self_attn(self.attn_desc, self.xa, self.aw["wq"], self.aw["wk"], self.aw["wv"],
+                          self.aw["wo"], self.kv[k0], self.kv[k1], self.ya, self.sa_ws,
+                          self.sa_ws_n, stream=s)
+        if core_events:
+            dpp.dpp_set_attn_core_events(None, None)
+        rec(3)
+        dpp.dpp_cross_attn(self.cross_desc, self.ya, self.ctx, self.xw["wq"], self.xw["wk"],
+                           self.xw["wv"], self.xw["wo"], self.yc, self.xa_ws, self.xa_ws_n,
+                           stream=s)
+        rec(4)
+        dpp.dpp_cfg_combine(self.u, self.c, w.cfg_scale, self.n_cfg, self.cfg_out, self.sums,
+                            self.cfg_ws, self.cfg_ws_n, stream=s)
+        rec(5)
+        dpp.dpp_refresh_stale(self.x, self.stale, c.B, c.H, self.row_bytes, c.P, stream=s)
+        rec(6)
+        self.i += 1
+
+    def h2d(self):
+        s = self.stream
+        self.x.copy_(self.host_x, non_blocking=True)
+        self.xa.copy_(self.host_xa, non_blocking=True)
+        self.ctx.copy_(self.host_ctx, non_blocking=True)
+        self.u.copy_(self.host_u, non_blocking=True)
+        self.c.copy_(self.host_c, non_blocking=True)
+        return sum(t.numel() * t.element_size() for t in
+                   (self.host_x, self.host_xa, self.host_ctx, self.host_u, self.host_c))
+
+    def alloc_d2h(self):
+        self.out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                         for t in (self.y2, self.yc, self.cfg_out, self.sums)]
+        return sum(t.numel() * t.element_size() for t in self.out_host)
+
+    def d2h(self):
+        for h, d in zip(self.out_host, (self.y2, self.yc, self.cfg_out, self.sums)):
+            h.copy_(d, non_blocking=True)
+
+
+# ------------------------------------------------------------------ oracle arm
+class OracleSample:
+    """Times the fp64 oracle on a bounded sample of the workload: conv output
+    rows at band edges and inside, and queries of one band of self- and
+    cross-attention (keys/values of that band's composite are projected in
+    full).  The full-size fp64 inputs are drawn once, outside the timing."""
+
+    def __init__(self, w):
+        import oracle
+        self.oracle, self.w = oracle, w
+        c, a = w.conv, w.attn
+        shape = (c.B, c.H, c.W, c.C)
+        self.F = wl.to_f64(wl.normal(shape, wl.seed_of(w.index, 0, wl.T_FRESH), dtype=w.dtype))
+        self.S = wl.to_f64(wl.perturbed(wl.normal(shape, wl.seed_of(w.index, 0, wl.T_FRESH),
+                                                  dtype=w.dtype),
+                                        wl.seed_of(w.index, 1, wl.T_STALE_NOISE), w.stale_scale))
+        self.Wt = wl.to_f64(wl.conv_weight(c.C, c.C, wl.seed_of(w.index, 0, wl.T_CONV_W),
+                                           w.dtype))
+        X = wl.normal((a.B, a.N, a.C), wl.seed_of(w.index, 0, wl.T_ATTN_X), dtype=w.dtype)
+        self.X = wl.to_f64(X[:1])
+        self.Xs = wl.to_f64(wl.perturbed(X, wl.seed_of(w.index, 1, wl.T_ATTN_X),
+                                         w.stale_scale)[:1])
+        self.aw = {k: wl.to_f64(v) for k, v in wl.attn_weights(a, w.index, w.dtype).items()}
+        self.xw = {k: wl.to_f64(v) for k, v in wl.cross_weights(a, w.index, w.dtype).items()}
+        self.ctx = wl.to_f64(wl.context(a, w.index, w.dtype)[:1])
+        self.rng = np.random.default_rng(7)
+
+    def run(self, sample_rows=8, sample_queries=48):
+        """Returns (tensor FLOPs of the sampled outputs, seconds, description)."""
+        o, w, rng = self.oracle, self.w, self.rng
+        c, a = w.conv, w.attn
+        Hp, Np = c.H // c.P, a.N // a.P
+        rows = sorted(set([Hp, 2 * Hp - 1] + list(rng.integers(0, c.H, sample_rows - 2))))
+        p = int(rng.integers(0, a.P))
+        qs = np.sort(rng.choice(np.arange(p * Np, (p + 1) * Np), sample_queries, replace=False))
+        t0 = time.perf_counter()
+        o.displaced_conv3x3(self.F, self.S, self.Wt, None, c.P, out_rows=rows)
+        o.displaced_self_attention(self.X, self.Xs, self.aw["wq"], self.aw["wk"], self.aw["wv"],
+                                   self.aw["wo"], a.heads, a.P, queries=qs)
+        o.cross_attention(self.X, self.ctx, self.xw["wq"], self.xw["wk"], self.xw["wv"],
+                          self.xw["wo"], a.heads, queries=qs)
+        secs = time.perf_counter() - t0
+        conv_f = 2.0 * c.B * len(rows) * c.W * c.C * 9 * c.C
+        nq = len(qs)
+        self_f = (4.0 * nq * a.N * a.head_dim * a.heads    # core for the sampled queries
+                  + 2.0 * a.N * a.C * 2 * a.C               # K/V of the band's composite
+                  + 2.0 * 2.0 * nq * a.C * a.C)             # Q and O projections
+        cross_f = (4.0 * nq * a.n_ctx * a.head_dim * a.heads + 2.0 * a.n_ctx * a.c_ctx * 2 * a.C
+                   + 2.0 * 2.0 * nq * a.C * a.C)
+        desc = (f"{len(rows)} conv output rows x batch {c.B}; {nq} queries of one band, "
+                f"batch 0, for self-attention (K/V of the band's composite projected in "
+                f"full) and cross-attention; fp64 numpy; per-step sample")
+        return conv_f + self_f + cross_f, secs, desc
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("internal_api") in
+             ("openblas", "mkl", "blis")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ main
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return 0
+    model = work_model(w)
+    sample = OracleSample(w)
+    for _ in range(args.warmup):
+        sample.run(4, 16)
+    flops, secs = 0.0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, t, desc = sample.run(4, 16)
+        flops += f
+        secs += t
+    val = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step_tflop_full": model["step_flop"] / 1e12},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = wl.WORKLOADS[WORKLOAD]
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, w, ws, rank)
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    import displaced_patch_parallelism_02_b300 as dpp
+    model = work_model(w)
+    peaks, peak_src = load_peaks()
+
+    step = Step(w, dev)
+    s = step.stream
+    for _ in range(max(args.warmup, 0)):
+        step.run()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    core = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = dpp.dpp_launch_count()
+    t_start.record(s)
+    for k in range(K):
+        step.run(evs[k], core[k])
+    t_end.record(s)
+    torch.cuda.synchronize(dev)
+    launches = dpp.dpp_launch_count() - launches0
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / K
+    value = model["step_flop"] * ws * K / (total_ms / 1e3) / 1e12
+
+    op_ms = {op: sum(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(K)) / K
+             for j, op in enumerate(step.ops)}
+    core_ms = sum(a.elapsed_time(b) for a, b in core) / K
+    tf = lambda f, ms: f / (ms / 1e3) / 1e12
+    gb = lambda b, ms: b / (ms / 1e3) / 1e9
+    sus = peaks["bf16_tflops_sustained"]
+    ops = {
+        "conv": {"ms": op_ms["conv"], "tflops": tf(model["conv_flop"], op_ms["conv"])},
+        "groupnorm": {"ms": op_ms["groupnorm"], "gbs": gb(model["gn_bytes"], op_ms["groupnorm"])},
+        "self_attn": {"ms": op_ms["self_attn"],
+                      "tflops": tf(model["self_core_flop"] + model["self_proj_flop"],
+                                   op_ms["self_attn"])},
+        "self_attn_core": {"ms": core_ms, "tflops": tf(model["self_core_flop"], core_ms)},
+        "cross_attn": {"ms": op_ms["cross_attn"],
+                       "tflops": tf(model["cross_flop"], op_ms["cross_attn"])},
+        "cfg": {"ms": op_ms["cfg"], "gbs": gb(model["cfg_bytes"], op_ms["cfg"])},
+        "refresh": {"ms": op_ms["refresh"], "gbs": gb(model["refresh_bytes"], op_ms["refresh"])},
+    }
+    for k, v in ops.items():
+        if "tflops" in v:
+            v["frac_of_sustained_bf16"] = v["tflops"] / sus
+        else:
+            v["frac_of_hbm"] = v["gbs"] / peaks["hbm_gbs"]
+
+    # end to end: pinned host inputs -> device, step, results -> host
+    bi = bo = 0
+    e2e_val = None
+    if K > 0:
+        bo = step.alloc_d2h()
+        torch.cuda.synchronize(dev)
+        if pg:
+            pg.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(K):
+            bi = step.h2d()
+            step.run()
+            step.d2h()
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if pg:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e_val = model["step_flop"] * ws * K / (e2e_ms / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        f, secs, desc = OracleSample(w).run()
+        cpu = {"value": f / secs / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+               "kind": "oracle", "sample": desc, "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+            "config": {"workload": WORKLOAD, "latent": [2, 480, 480, 320], "bands": 8,
+                       "attn_tokens": [2, 57600], "attn_channels": 640, "heads": 10,
+                       "text_ctx": [77, 2048], "cfg_maps": [2, 4, 480, 480],
+                       "parallelism": f"replicas{ws}",
+                       "l2": "no flush: inputs and step working set exceed the 126 MB L2"},
+            "roofline": {"kernel": "self-attention core", "bound": "tensor",
+                         "achieved": ops["self_attn_core"]["tflops"], "peak": sus,
+                         "unit": "TFLOP/s", "frac": ops["self_attn_core"]["tflops"] / sus,
+                         "peak_source": f"{peak_src} bf16 sustained", "traffic": None},
+            "ops": ops,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+                    "d2h_bytes_per_step": bo},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,332 @@
+// C-ABI entry points of libdpp.so (declared in include/dpp.h).
+//
+// Every entry point validates its arguments on the host -- before any CUDA
+// call -- and returns a dpp_status without launching anything when they are
+// wrong.  The library allocates no device memory: workspaces come from the
+// caller, sized by the *_workspace_bytes() queries.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+
+#include "dpp_internal.h"
+
+namespace dpp {
+
+__device__ int g_device_status;
+
+int *device_status_ptr() {
+  static int *cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = reinterpret_cast<int *>(p);
+  }
+  return cache[dev];
+}
+
+}  // namespace dpp
+
+using namespace dpp;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+size_t elem_size(dpp_dtype t) { return t == DPP_BF16 ? 2 : 4; }
+
+bool dtype_ok(dpp_dtype t) { return t == DPP_F32 || t == DPP_BF16; }
+
+// channel granularity of the 16-byte vector paths
+int chan_quantum(dpp_dtype t) { return t == DPP_BF16 ? 8 : 4; }
+
+dpp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DPP_OK : DPP_ERR_CUDA; }
+
+constexpr long long kMaxElems = (1ll << 31) - 1;
+
+dpp_status check_conv(const dpp_conv_desc *d, const void *x, const void *stale, const void *w,
+                      const float *bias, const void *y) {
+  if (!d || !x || !w || !y) return DPP_ERR_INVALID_ARG;
+  if (!dtype_ok(d->dtype)) return DPP_ERR_INVALID_ARG;
+  if (d->B < 1 || d->H < 1 || d->W < 1 || d->C_in < 1 || d->C_out < 1 || d->P < 1)
+    return DPP_ERR_INVALID_ARG;
+  if (d->H % d->P != 0) return DPP_ERR_INVALID_ARG;
+  const int q = chan_quantum(d->dtype);
+  if (d->C_in % q || d->C_out % q) return DPP_ERR_INVALID_ARG;
+  const long long pix = (long long)d->B * d->H * d->W;
+  if (pix * d->C_in > kMaxElems || pix * d->C_out > kMaxElems) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (stale && !aligned16(stale)) ||
+      (bias && !aligned16(bias)))
+    return DPP_ERR_ALIGN;
+  const size_t es = elem_size(d->dtype);
+  const size_t nx = (size_t)pix * d->C_in * es, ny = (size_t)pix * d->C_out * es;
+  if (overlap(y, ny, x, nx) || overlap(y, ny, stale, nx) ||
+      overlap(y, ny, w, (size_t)d->C_out * 9 * d->C_in * es))
+    return DPP_ERR_ALIAS;
+  return DPP_OK;
+}
+
+dpp_status check_gn(const dpp_gn_desc *d) {
+  if (!d || !dtype_ok(d->dtype)) return DPP_ERR_INVALID_ARG;
+  if (d->B < 1 || d->H < 1 || d->W < 1 || d->C < 1 || d->G < 1 || d->P < 1)
+    return DPP_ERR_INVALID_ARG;
+  if (d->H % d->P != 0 || d->C % d->G != 0) return DPP_ERR_INVALID_ARG;
+  if (!(d->eps >= 0.f)) return DPP_ERR_INVALID_ARG;
+  const int q = chan_quantum(d->dtype);
+  if (d->C % q) return DPP_ERR_INVALID_ARG;
+  if (d->C / q > 1024) return DPP_ERR_UNSUPPORTED;
+  if ((long long)d->B * d->H * d->W * d->C > kMaxElems) return DPP_ERR_UNSUPPORTED;
+  return DPP_OK;
+}
+
+dpp_status check_attn(const dpp_attn_desc *d, bool cross) {
+  if (!d || !dtype_ok(d->dtype)) return DPP_ERR_INVALID_ARG;
+  if (d->B < 1 || d->H < 1 || d->W < 1 || d->C < 1 || d->heads < 1 || d->P < 1)
+    return DPP_ERR_INVALID_ARG;
+  if (d->head_dim != 64) return DPP_ERR_UNSUPPORTED;
+  if (d->C != d->heads * d->head_dim) return DPP_ERR_INVALID_ARG;
+  if (d->H % d->P != 0) return DPP_ERR_INVALID_ARG;
+  if (cross) {
+    if (d->n_ctx < 1 || d->c_ctx < 1) return DPP_ERR_INVALID_ARG;
+    if (d->c_ctx % 8) return DPP_ERR_INVALID_ARG;
+  }
+  const long long N = (long long)d->H * d->W;
+  if ((long long)d->B * N * 3 * d->C > kMaxElems) return DPP_ERR_UNSUPPORTED;
+  return DPP_OK;
+}
+
+size_t attn_tokens(const dpp_attn_desc &d) { return (size_t)d.B * d.H * d.W; }
+
+std::atomic<uint64_t> g_launches{0};
+cudaEvent_t g_core_start = nullptr, g_core_stop = nullptr;
+
+// Counts the kernels of a launcher call that returned cudaSuccess.
+cudaError_t counted(cudaError_t e, int kernels) {
+  if (e == cudaSuccess) g_launches += (uint64_t)kernels;
+  return e;
+}
+
+// Launches the attention core, bracketed by the profiling events when set.
+cudaError_t attn_core(const AttnArgs &a, cudaStream_t s) {
+  if (g_core_start && g_core_stop) cudaEventRecord(g_core_start, s);
+  cudaError_t e = counted(launch_attn_simt(a, s), 1);
+  if (g_core_start && g_core_stop) cudaEventRecord(g_core_stop, s);
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dpp_status_string(dpp_status s) {
+  switch (s) {
+    case DPP_OK: return "DPP_OK";
+    case DPP_ERR_INVALID_ARG: return "DPP_ERR_INVALID_ARG";
+    case DPP_ERR_UNSUPPORTED: return "DPP_ERR_UNSUPPORTED";
+    case DPP_ERR_ALIAS: return "DPP_ERR_ALIAS";
+    case DPP_ERR_WORKSPACE: return "DPP_ERR_WORKSPACE";
+    case DPP_ERR_CUDA: return "DPP_ERR_CUDA";
+    case DPP_ERR_TIMEOUT: return "DPP_ERR_TIMEOUT";
+    case DPP_ERR_ALIGN: return "DPP_ERR_ALIGN";
+  }
+  return "DPP_ERR_UNKNOWN";
+}
+
+int dpp_version(void) { return 100; }
+
+uint64_t dpp_launch_count(void) { return g_launches.load(); }
+
+void dpp_set_attn_core_events(void *start, void *stop) {
+  g_core_start = (cudaEvent_t)start;
+  g_core_stop = (cudaEvent_t)stop;
+}
+
+dpp_status dpp_device_status(dpp_stream stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DPP_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return DPP_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return DPP_ERR_CUDA;
+  return (dpp_status)v;
+}
+
+// ------------------------------------------------------------------ refresh
+dpp_status dpp_refresh_stale(const void *fresh, void *stale, size_t outer, size_t rows,
+                             size_t row_bytes, int P, uint64_t patch_mask, dpp_stream stream) {
+  if (!fresh || !stale) return DPP_ERR_INVALID_ARG;
+  if (P < 1 || P > 64 || rows == 0 || outer == 0 || rows % (size_t)P) return DPP_ERR_INVALID_ARG;
+  if (row_bytes == 0 || row_bytes % 16) return DPP_ERR_INVALID_ARG;
+  if (!aligned16(fresh) || !aligned16(stale)) return DPP_ERR_ALIGN;
+  const size_t total = outer * rows * row_bytes;
+  if (total / outer / rows != row_bytes) return DPP_ERR_INVALID_ARG;  // overflow
+  if (overlap(fresh, total, stale, total)) return DPP_ERR_ALIAS;
+  if (P < 64) patch_mask &= (1ull << P) - 1;
+  if (patch_mask == 0) return DPP_OK;
+  return from_cuda(counted(launch_refresh(fresh, stale, outer, rows, row_bytes, P, patch_mask,
+                                          (cudaStream_t)stream), 1));
+}
+
+// ---------------------------------------------------------------------- CFG
+size_t dpp_cfg_workspace_bytes(size_t n) { return 16 + cfg_blocks(n) * 3 * sizeof(double); }
+
+dpp_status dpp_cfg_combine(const float *eps_u, const float *eps_c, float scale, size_t n,
+                           float *out, double *sums3, void *ws, size_t ws_bytes,
+                           dpp_stream stream) {
+  if (n > 0 && (!eps_u || !eps_c || !out)) return DPP_ERR_INVALID_ARG;
+  if (n > ((size_t)1 << 40)) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(eps_u) || !aligned16(eps_c) || !aligned16(out) ||
+      (sums3 && ((uintptr_t)sums3 & 7u)))
+    return DPP_ERR_ALIGN;
+  const size_t nb = n * sizeof(float);
+  if ((out != eps_u && overlap(out, nb, eps_u, nb)) || (out != eps_c && overlap(out, nb, eps_c, nb)))
+    return DPP_ERR_ALIAS;
+  if (sums3) {
+    if (!ws || ws_bytes < dpp_cfg_workspace_bytes(n)) return DPP_ERR_WORKSPACE;
+    if (!aligned16(ws)) return DPP_ERR_ALIGN;
+    if (overlap(ws, ws_bytes, sums3, 3 * sizeof(double))) return DPP_ERR_ALIAS;
+  }
+  return from_cuda(
+      counted(launch_cfg(eps_u, eps_c, scale, n, out, sums3, ws, (cudaStream_t)stream), 1));
+}
+
+// ---------------------------------------------------------------- groupnorm
+size_t dpp_groupnorm_workspace_bytes(const dpp_gn_desc *d) {
+  if (check_gn(d) != DPP_OK) return 0;
+  return gn_workspace(*d);
+}
+
+dpp_status dpp_groupnorm(const dpp_gn_desc *d, const void *x, const float *stats_prev,
+                         float *stats_next, const float *gamma, const float *beta, void *y,
+                         void *ws, size_t ws_bytes, dpp_stream stream) {
+  dpp_status st = check_gn(d);
+  if (st != DPP_OK) return st;
+  if (!x || !y || !stats_next) return DPP_ERR_INVALID_ARG;
+  if ((gamma == nullptr) != (beta == nullptr)) return DPP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(stats_next) ||
+      (stats_prev && !aligned16(stats_prev)))
+    return DPP_ERR_ALIGN;
+  const size_t need = gn_workspace(*d);
+  if (!ws || ws_bytes < need) return DPP_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPP_ERR_ALIGN;
+  const size_t nx = (size_t)d->B * d->H * d->W * d->C * elem_size(d->dtype);
+  const size_t ns = (size_t)d->P * d->B * d->G * 2 * sizeof(float);
+  if (y != x && overlap(y, nx, x, nx)) return DPP_ERR_ALIAS;
+  if (overlap(stats_prev, ns, stats_next, ns)) return DPP_ERR_ALIAS;
+  if (overlap(ws, need, x, nx) || overlap(ws, need, y, nx) || overlap(ws, need, stats_next, ns) ||
+      overlap(stats_next, ns, y, nx))
+    return DPP_ERR_ALIAS;
+  return from_cuda(counted(launch_groupnorm(*d, x, stats_prev, stats_next, gamma, beta, y, ws,
+                                            (cudaStream_t)stream), 2));
+}
+
+// --------------------------------------------------------------------- conv
+dpp_status dpp_conv3x3(const dpp_conv_desc *d, const void *x, const void *stale_prev,
+                       const void *w, const float *bias, void *y, dpp_stream stream) {
+  dpp_status st = check_conv(d, x, stale_prev, w, bias, y);
+  if (st != DPP_OK) return st;
+  return from_cuda(
+      counted(launch_conv_simt(*d, x, stale_prev, w, bias, y, (cudaStream_t)stream), 1));
+}
+
+// ---------------------------------------------------------------- attention
+size_t dpp_self_attn_workspace_bytes(const dpp_attn_desc *d) {
+  if (check_attn(d, false) != DPP_OK) return 0;
+  const size_t n = attn_tokens(*d) * d->C * elem_size(d->dtype);
+  return 2 * align_up(n, 256);  // Q, O
+}
+
+size_t dpp_cross_attn_workspace_bytes(const dpp_attn_desc *d) {
+  if (check_attn(d, true) != DPP_OK) return 0;
+  const size_t es = elem_size(d->dtype);
+  const size_t n = attn_tokens(*d) * d->C * es;
+  const size_t kv = (size_t)d->B * d->n_ctx * 2 * d->C * es;
+  return 2 * align_up(n, 256) + align_up(kv, 256);  // Q, O, context K/V
+}
+
+dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, const void *wk,
+                         const void *wv, const void *wo, const void *kv_prev, void *kv_next,
+                         void *y, void *ws, size_t ws_bytes, dpp_stream stream) {
+  dpp_status st = check_attn(d, false);
+  if (st != DPP_OK) return st;
+  if (!x || !wq || !wk || !wv || !wo || !kv_next || !y) return DPP_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, wq, wk, wv, wo, kv_next, y, ws};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return DPP_ERR_ALIGN;
+  if (kv_prev && !aligned16(kv_prev)) return DPP_ERR_ALIGN;
+  const size_t need = dpp_self_attn_workspace_bytes(d);
+  if (!ws || ws_bytes < need) return DPP_ERR_WORKSPACE;
+  const size_t es = elem_size(d->dtype);
+  const size_t nt = attn_tokens(*d);
+  const size_t nx = nt * d->C * es, nkv = nt * 2 * d->C * es;
+  if (overlap(kv_prev, nkv, kv_next, nkv)) return DPP_ERR_ALIAS;
+  if (overlap(y, nx, kv_next, nkv) || overlap(y, nx, kv_prev, nkv) || overlap(ws, need, y, nx) ||
+      overlap(ws, need, x, nx) || overlap(ws, need, kv_next, nkv) ||
+      overlap(ws, need, kv_prev, nkv) || overlap(x, nx, kv_next, nkv))
+    return DPP_ERR_ALIAS;
+  if (y != x && overlap(y, nx, x, nx)) return DPP_ERR_ALIAS;
+  cudaStream_t s = (cudaStream_t)stream;
+  char *wsb = reinterpret_cast<char *>(ws);
+  void *q = wsb;
+  void *o = wsb + align_up(nx, 256);
+  const int C = d->C;
+  const int M = (int)nt;
+  // 1. Q for every token (every band's own queries), fresh K/V into kv_next
+  GemmArgs qkv{x, {wq, wk, wv}, C, M, 3 * C, C, q, C, C, kv_next, 2 * C, d->dtype};
+  cudaError_t e = counted(launch_gemm_simt(qkv, s), 1);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  // 2. displaced attention core
+  AttnArgs a{q, kv_next, kv_prev, o, d->B, d->H * d->W, d->H * d->W, C, d->heads, d->P,
+             d->dtype};
+  e = attn_core(a, s);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  // 3. output projection
+  GemmArgs op{o, {wo, nullptr, nullptr}, C, M, C, C, y, C, C, nullptr, 0, d->dtype};
+  return from_cuda(counted(launch_gemm_simt(op, s), 1));
+}
+
+dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx, const void *wq,
+                          const void *wk, const void *wv, const void *wo, void *y, void *ws,
+                          size_t ws_bytes, dpp_stream stream) {
+  dpp_status st = check_attn(d, true);
+  if (st != DPP_OK) return st;
+  if (!x || !ctx || !wq || !wk || !wv || !wo || !y) return DPP_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, ctx, wq, wk, wv, wo, y, ws};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return DPP_ERR_ALIGN;
+  const size_t need = dpp_cross_attn_workspace_bytes(d);
+  if (!ws || ws_bytes < need) return DPP_ERR_WORKSPACE;
+  const size_t es = elem_size(d->dtype);
+  const size_t nt = attn_tokens(*d);
+  const size_t nx = nt * d->C * es;
+  if (overlap(ws, need, y, nx) || overlap(ws, need, x, nx) ||
+      overlap(ws, need, ctx, (size_t)d->B * d->n_ctx * d->c_ctx * es))
+    return DPP_ERR_ALIAS;
+  if (y != x && overlap(y, nx, x, nx)) return DPP_ERR_ALIAS;
+  cudaStream_t s = (cudaStream_t)stream;
+  char *wsb = reinterpret_cast<char *>(ws);
+  void *q = wsb;
+  void *o = wsb + align_up(nx, 256);
+  void *kv = wsb + 2 * align_up(nx, 256);
+  const int C = d->C;
+  GemmArgs qg{x, {wq, nullptr, nullptr}, C, (int)nt, C, C, q, C, C, nullptr, 0, d->dtype};
+  cudaError_t e = counted(launch_gemm_simt(qg, s), 1);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  GemmArgs kvg{ctx, {wk, wv, nullptr}, C, d->B * d->n_ctx, 2 * C, d->c_ctx,
+               kv, 2 * C, 2 * C, nullptr, 0, d->dtype};
+  e = counted(launch_gemm_simt(kvg, s), 1);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  AttnArgs a{q, kv, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, d->dtype};
+  e = attn_core(a, s);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  GemmArgs op{o, {wo, nullptr, nullptr}, C, (int)nt, C, C, y, C, C, nullptr, 0, d->dtype};
+  return from_cuda(counted(launch_gemm_simt(op, s), 1));
+}
+
+}  // extern "C"

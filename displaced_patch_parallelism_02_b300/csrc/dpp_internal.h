@@ -1,0 +1,93 @@
+// Internal declarations shared by the translation units of libdpp.so.
+// Host-side launchers (one per kernel family) and small device helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dpp.h"
+
+namespace dpp {
+
+// ---------------------------------------------------------------- constants
+// Grid sizes of the reductions are fixed functions of the problem shape (not
+// of the device), so every reduction order -- and therefore every bit of the
+// results -- is the same on any GPU.
+constexpr int kReduceBlocks = 1184;  // 148 SMs x 8
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- launchers
+// All return cudaSuccess or the launch error; arguments were validated.
+
+// refresh: copy selected bands of [outer][rows][row_bytes] (row_bytes % 16 == 0)
+cudaError_t launch_refresh(const void *fresh, void *stale, size_t outer, size_t rows,
+                           size_t row_bytes, int P, uint64_t mask, cudaStream_t s);
+
+// guidance combine + discrepancy sums
+size_t cfg_blocks(size_t n);
+cudaError_t launch_cfg(const float *u, const float *c, float scale, size_t n, float *out,
+                       double *sums3, void *ws, cudaStream_t s);
+
+// GroupNorm: partial-sum pass and normalise pass
+struct GnPlan {
+  int units;          // P * B
+  int chunks;         // chunks per unit
+  int pix_per_unit;   // (H / P) * W
+  int pix_per_chunk;
+};
+GnPlan gn_plan(const dpp_gn_desc &d);
+size_t gn_workspace(const dpp_gn_desc &d);
+cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *stats_prev,
+                             float *stats_next, const float *gamma, const float *beta,
+                             void *y, void *ws, cudaStream_t s);
+
+// SIMT implicit-GEMM conv (fp32 / bf16 storage, fp32 math)
+cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *stale,
+                             const void *w, const float *bias, void *y, cudaStream_t s);
+
+// tcgen05 implicit-GEMM conv (bf16); returns cudaErrorNotSupported when the
+// shape is outside what the kernel handles
+cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *stale,
+                           const void *w, const float *bias, void *y, int *status,
+                           cudaStream_t s);
+
+// GEMM D = A * B^T with B given as up to 3 row blocks (weights [out, in]);
+// output columns [0, split) go to out0 (leading dim ld0), the rest to out1
+// (leading dim ld1, column index minus split).
+struct GemmArgs {
+  const void *A;      // [M, K]
+  const void *B[3];   // each [b_rows, K]
+  int b_rows;         // rows per B block
+  int M, N, K;
+  void *out0;
+  int ld0;
+  int split;
+  void *out1;
+  int ld1;
+  dpp_dtype dtype;
+};
+cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s);
+cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s);
+
+// attention core: O = softmax(Q K^T / 8) V for head_dim 64.
+// q: [B, Nq, C]; kv_fresh / kv_stale: [B, Nkv, 2, C] (kv_stale may be null:
+// everything fresh).  Query band p (of P) attends over fresh keys of its own
+// band and stale keys elsewhere; with Nkv != Nq (cross attention) P must be 1.
+struct AttnArgs {
+  const void *q;
+  const void *kv_fresh;
+  const void *kv_stale;
+  void *o;
+  int B, Nq, Nkv, C, heads, P;
+  dpp_dtype dtype;
+};
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s);
+
+// device status word (bounded waits record DPP_ERR_TIMEOUT here)
+int *device_status_ptr();
+
+}  // namespace dpp

@@ -1,0 +1,244 @@
+/*
+ * dpp.h -- C ABI of the displaced-patch-parallelism hot path (libdpp.so).
+ *
+ * Displaced patch parallelism ("DistriFusion: Distributed Parallel Inference
+ * for High-Resolution Diffusion Models", reader's notes, Introduction
+ * para. 4 and Related Work / Parallelism): an image latent is cut into P
+ * horizontal bands ("patches"), one per device.  At a displaced denoising
+ * step each band computes its own rows from fresh activations and takes the
+ * other bands' activations from the previous step (the stale buffer), so
+ * the exchange between devices can overlap compute.  The first step is
+ * synchronous (stale == fresh).  The layer wrappers are a 3x3 convolution
+ * (DistriConv2dPP), GroupNorm (DistriGroupNorm) and self/cross attention
+ * (DistriSelfAttentionPP, DistriCrossAttentionPP); the exchange is an
+ * all_gather of each band's rows concatenated along the height axis
+ * ("DistriFusion开发者必读：分布式UNet架构设计与模块拆分实现详解", sections
+ * 卷积层拆分, 归一化层拆分, 注意力机制拆分, 分布式通信与同步机制).
+ *
+ * This library runs all P bands on ONE GPU: band p is a "virtual device"
+ * inside each batched launch, and the all_gather becomes an in-HBM refresh
+ * of the stale buffer, normally written by the producing kernel itself.
+ * Every displaced op computes, for band p, the ordinary full-image layer
+ * applied to the composite image Z_p (fresh rows R_p = [p*H/P, (p+1)*H/P),
+ * stale rows elsewhere), restricted to R_p.
+ *
+ * Conventions for every entry point:
+ *   - Memory: all tensor pointers are DEVICE pointers owned by the caller,
+ *     16-byte aligned, dense (no strides).  The library never allocates
+ *     device memory and keeps no state between calls except a host-side
+ *     cache of TMA tensor maps keyed by (pointer, shape), a launch counter
+ *     and the optional profiling events of dpp_set_attn_core_events().  Workspace, where
+ *     needed, is passed in by the caller; its size comes from the matching
+ *     *_workspace_bytes() query.
+ *   - Layout: activations NHWC [B, H, W, C] (torch channels_last); attention
+ *     tokens [B, N, C] with N = H*W and token n = h*W + w, so band p owns
+ *     the contiguous tokens [p*N/P, (p+1)*N/P).  Channel c of an attention
+ *     layer belongs to head c / head_dim.
+ *   - Types: DPP_BF16 = bf16 storage, fp32 accumulation and softmax;
+ *     DPP_F32 = fp32 storage and arithmetic (SIMT path, no TF32).
+ *     Biases, GroupNorm affine and statistics are always fp32.
+ *   - Streams: every call is asynchronous on `stream` (a cudaStream_t;
+ *     NULL = legacy default stream).
+ *   - Errors: argument checks run on the host before anything is launched
+ *     and return a dpp_status with no side effect.  A failed launch returns
+ *     DPP_ERR_CUDA.  Kernels that wait on barriers give up after a bounded
+ *     time and record DPP_ERR_TIMEOUT in a device status word read by
+ *     dpp_device_status().
+ *   - Synchronous step: passing NULL as the stale input (stale_prev,
+ *     stats_prev, kv_prev) means "all bands are fresh" -- the synchronous
+ *     first step, which is exactly the unpartitioned full-image layer.
+ *   - Stale inputs and the *_next outputs that refresh them must not
+ *     overlap (DPP_ERR_ALIAS): band q's refresh would otherwise overwrite
+ *     data band p still reads in the same launch.
+ */
+#ifndef DPP_H_
+#define DPP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *dpp_stream;
+
+typedef enum {
+  DPP_OK = 0,
+  DPP_ERR_INVALID_ARG = 1, /* null pointer, bad size, H % P != 0, ... */
+  DPP_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head_dim != 64) */
+  DPP_ERR_ALIAS = 3,       /* a stale input overlaps the buffer refreshing it */
+  DPP_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  DPP_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+  DPP_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up */
+  DPP_ERR_ALIGN = 7        /* a pointer is not 16-byte aligned */
+} dpp_status;
+
+typedef enum { DPP_F32 = 0, DPP_BF16 = 1 } dpp_dtype;
+
+/* 3x3 conv, stride 1, zero padding 1, C_in -> C_out.
+ * first_layer: the conv_in flag of the conv wrapper (is_first_layer); the
+ * input latent is identical on every device, so the halo is fresh and
+ * stale_prev is ignored. */
+typedef struct {
+  int B, H, W, C_in, C_out, P;
+  dpp_dtype dtype;
+  int first_layer;
+} dpp_conv_desc;
+
+/* GroupNorm over [B, H, W, C] with G groups of C/G consecutive channels. */
+typedef struct {
+  int B, H, W, C, G, P;
+  float eps;
+  dpp_dtype dtype;
+} dpp_gn_desc;
+
+/* Attention over an H x W token grid (N = H*W), C = heads * head_dim.
+ * n_ctx / c_ctx: text-context length and width (cross-attention only). */
+typedef struct {
+  int B, H, W, C, heads, head_dim, P;
+  int n_ctx, c_ctx;
+  dpp_dtype dtype;
+} dpp_attn_desc;
+
+/* ---------------------------------------------------------------------------
+ * dpp_conv3x3 -- DistriConv2dPP (section 卷积层拆分 of the DistriFusion
+ * developer guide; displaced semantics from the reader's notes, Introduction
+ * para. 4).
+ *   y[b,h,w,o] = bias[o] + sum_{i,dy,dx} w[o,dy,dx,i] * Z_p[b,h+dy-1,w+dx-1,i]
+ * for h in band p, Z_p = x on the band's rows and stale_prev elsewhere
+ * (only the rows just above and below the band are read from stale_prev),
+ * zero outside the image.
+ *   x, stale_prev, y : [B, H, W, C_in/C_out] NHWC, desc->dtype.
+ *                      stale_prev == NULL or == x: synchronous step.
+ *   w                : [C_out, 3, 3, C_in] (torch [C_out, C_in, 3, 3] in
+ *                      channels_last memory), desc->dtype.
+ *   bias             : [C_out] fp32 or NULL.
+ * Requires H % P == 0, C_in and C_out multiples of 8 (bf16) / 4 (f32).
+ * y must not overlap x or stale_prev.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_conv3x3(const dpp_conv_desc *desc, const void *x, const void *stale_prev,
+                       const void *w, const float *bias, void *y, dpp_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * dpp_groupnorm -- DistriGroupNorm (section 归一化层拆分 of the DistriFusion
+ * developer guide).  Per band p, batch b, group g:
+ *   s1 = sum over band p of x  +  sum_{q != p} stats_prev[q,b,g,0]
+ *   s2 = likewise for x^2,  n = H*W*C/G,  mean = s1/n,
+ *   var = max(s2/n - mean^2, 0) (biased),
+ *   y = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c]   on band p's rows.
+ * The band's fresh partials (sum x, sum x^2) are written to stats_next[p]
+ * in the same call: that write is the refresh of the GroupNorm state.
+ *   x, y        : [B, H, W, C] NHWC, desc->dtype; y may equal x (in place).
+ *   stats_prev  : [P, B, G, 2] fp32, the previous step's stats_next, or NULL
+ *                 for the synchronous step (statistics of x alone).
+ *   stats_next  : [P, B, G, 2] fp32 output; must not overlap stats_prev.
+ *   gamma, beta : [C] fp32, both NULL for no affine.
+ *   ws          : dpp_groupnorm_workspace_bytes(desc) bytes of device memory.
+ * Requires H % P == 0, C % G == 0, C a multiple of 8 (bf16) / 4 (f32).
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_groupnorm(const dpp_gn_desc *desc, const void *x, const float *stats_prev,
+                         float *stats_next, const float *gamma, const float *beta, void *y,
+                         void *ws, size_t ws_bytes, dpp_stream stream);
+size_t dpp_groupnorm_workspace_bytes(const dpp_gn_desc *desc);
+
+/* ---------------------------------------------------------------------------
+ * dpp_self_attn -- DistriSelfAttentionPP (section 注意力机制拆分 of the
+ * DistriFusion developer guide, attn1).  For band p:
+ *   Q = x[band p] wq^T;  K/V rows of band p's tokens are x[band p] wk^T /
+ *   x[band p] wv^T (fresh), all other rows come from kv_prev (stale);
+ *   O = softmax(Q K^T / sqrt(head_dim)) V per head;  y[band p] = O wo^T.
+ * The fresh K/V of every token are written to kv_next by the projection
+ * kernel itself: that write is the refresh of the attention state.
+ *   x, y     : [B, N, C] tokens, desc->dtype.
+ *   wq..wo   : [C, C] torch Linear [out, in], desc->dtype, no bias.
+ *   kv_prev  : [B, N, 2, C] (K then V per token) from the previous step,
+ *              or NULL for the synchronous step.
+ *   kv_next  : [B, N, 2, C] output; must not overlap kv_prev.
+ *   ws       : dpp_self_attn_workspace_bytes(desc) bytes (Q and O).
+ * Requires head_dim == 64, H % P == 0, C == heads * 64.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_self_attn(const dpp_attn_desc *desc, const void *x, const void *wq,
+                         const void *wk, const void *wv, const void *wo,
+                         const void *kv_prev, void *kv_next, void *y, void *ws,
+                         size_t ws_bytes, dpp_stream stream);
+size_t dpp_self_attn_workspace_bytes(const dpp_attn_desc *desc);
+
+/* ---------------------------------------------------------------------------
+ * dpp_cross_attn -- DistriCrossAttentionPP (attn2).  The text context is
+ * replicated on every device, so no stale state enters:
+ *   Q = x wq^T, K = ctx wk^T, V = ctx wv^T,
+ *   y = softmax(Q K^T / sqrt(head_dim)) V wo^T.
+ *   x, y   : [B, N, C];  ctx : [B, n_ctx, c_ctx];  desc->dtype.
+ *   wq, wo : [C, C];  wk, wv : [C, c_ctx].
+ *   ws     : dpp_cross_attn_workspace_bytes(desc) bytes.
+ * Requires head_dim == 64, c_ctx a multiple of 8.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_cross_attn(const dpp_attn_desc *desc, const void *x, const void *ctx,
+                          const void *wq, const void *wk, const void *wv, const void *wo,
+                          void *y, void *ws, size_t ws_bytes, dpp_stream stream);
+size_t dpp_cross_attn_workspace_bytes(const dpp_attn_desc *desc);
+
+/* ---------------------------------------------------------------------------
+ * dpp_cfg_combine -- classifier-free-guidance combine and the denoising
+ * discrepancy of the Hydiff summaries (gist.science, "基于条件的数据划分"
+ * and "自适应并行切换"; Avetisyan, "Адаптивное переключение"):
+ *   out[i] = eps_u[i] + scale * (eps_c[i] - eps_u[i])
+ *   sums3  = { sum|eps_c - eps_u|, sum|eps_u|, sum|eps_c| }   (fp64)
+ * rel-MAE = sums3[0] / sums3[1].  The reduction order is fixed, so sums3 is
+ * bit-reproducible for a given n.
+ *   eps_u, eps_c, out : n fp32 (out may equal eps_u or eps_c).
+ *   sums3             : 3 doubles of device memory, or NULL.
+ *   ws                : dpp_cfg_workspace_bytes(n) bytes.  Its first 16
+ *                       bytes are a completion counter that must be zero
+ *                       before the first call (e.g. cudaMemset); every call
+ *                       that completes leaves it zero again.  Calls that
+ *                       share a workspace must not overlap on the GPU.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_cfg_combine(const float *eps_u, const float *eps_c, float scale, size_t n,
+                           float *out, double *sums3, void *ws, size_t ws_bytes,
+                           dpp_stream stream);
+size_t dpp_cfg_workspace_bytes(size_t n);
+
+/* ---------------------------------------------------------------------------
+ * dpp_refresh_stale -- the all_gather of the gathered-buffer exchange
+ * (section 分布式通信与同步机制 of the DistriFusion developer guide):
+ * bands are concatenated along the height axis.  The tensor is viewed as
+ * [outer][rows][row_bytes]; band p owns rows [p*rows/P, (p+1)*rows/P) of
+ * every outer slice.  For every p whose bit is set in patch_mask the band is
+ * copied bit-exactly from fresh to stale; other bands are left untouched.
+ *   NHWC activations : outer = B, rows = H, row_bytes = W*C*elem
+ *   K/V state        : outer = B, rows = N, row_bytes = 2*C*elem
+ *   GroupNorm stats  : outer = 1, rows = P, row_bytes = B*G*2*4
+ * Requires rows % P == 0, 1 <= P <= 64, row_bytes % 16 == 0; fresh and
+ * stale must not overlap.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_refresh_stale(const void *fresh, void *stale, size_t outer, size_t rows,
+                             size_t row_bytes, int P, uint64_t patch_mask, dpp_stream stream);
+
+/* Reads and clears the device status word written by bounded waits
+ * (DPP_OK or DPP_ERR_TIMEOUT).  Synchronises `stream`. */
+dpp_status dpp_device_status(dpp_stream stream);
+
+/* Number of kernels this library has launched in this process (monotonic).
+ * Calls rejected by argument checks launch nothing and leave it unchanged. */
+uint64_t dpp_launch_count(void);
+
+/* Profiling hook.  When start and stop are both non-NULL (cudaEvent_t
+ * values), every later dpp_self_attn / dpp_cross_attn call records `start`
+ * on its stream immediately before launching its attention-core kernel and
+ * `stop` immediately after; pass NULL, NULL to turn it off.  Process-global
+ * and not thread-safe: meant for a benchmark timing that one kernel live. */
+void dpp_set_attn_core_events(void *start, void *stop);
+
+/* Human-readable name of a status code (static storage). */
+const char *dpp_status_string(dpp_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dpp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DPP_H_ */

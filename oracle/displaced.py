@@ -155,12 +155,13 @@ def groupnorm_partials(X, G, P):
     return out
 
 
-def displaced_groupnorm(F, S, G, eps, gamma, beta, P):
+def displaced_groupnorm(F, S, G, eps, gamma, beta, P, bands=None):
     """Displaced GroupNorm: band p's rows of groupnorm(Z_p).  Returns the full
-    ``[B, H, W, C]`` output (band p filled from its own composite)."""
+    ``[B, H, W, C]`` output (band p filled from its own composite); with
+    ``bands`` only those bands are evaluated and the other rows are NaN."""
     B, H, W, C = F.shape
-    out = np.empty((B, H, W, C))
-    for p in range(P):
+    out = np.full((B, H, W, C), np.nan)
+    for p in (range(P) if bands is None else bands):
         lo, hi = patch_rows(H, P, p)
         out[:, lo:hi] = groupnorm(composite(F, S, P, p), G, eps, gamma, beta)[:, lo:hi]
     return out

@@ -1,0 +1,115 @@
+"""Test helpers that run one op through the C ABI (ctypes binding) on cuda:0.
+
+Inputs are CPU torch tensors from ``workloads``; outputs come back as CPU
+tensors.  Nothing here computes any part of the method: it allocates device
+buffers, builds descriptors and calls the library.
+"""
+import numpy as np
+import torch
+
+import displaced_patch_parallelism_02_b300 as dpp
+
+CODES = {torch.float32: dpp.DPP_F32, torch.bfloat16: dpp.DPP_BF16}
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}  # max-abs error / RMS of the output
+
+
+def cuda(t):
+    return None if t is None else t.contiguous().to("cuda")
+
+
+def f64(t):
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def assert_rms_close(got, want, rel, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    rms = float(np.sqrt(np.mean(want ** 2)))
+    err = float(np.max(np.abs(got - want))) if got.size else 0.0
+    assert err <= rel * rms, f"{what}: max|err| {err:.4g} > {rel} x RMS {rms:.4g}"
+    return err / rms if rms else 0.0
+
+
+# ---------------------------------------------------------------- conv
+def conv(x, stale, w, bias, P, first_layer=False, stream=None):
+    """x, stale: [B,H,W,Ci] (device or CPU); w: [Co,Ci,3,3] torch order."""
+    x = cuda(x)
+    stale = cuda(stale) if stale is not None and stale.device.type == "cpu" else stale
+    B, H, W, Ci = x.shape
+    Co = w.shape[0]
+    wd = cuda(w.permute(0, 2, 3, 1))  # [Co,3,3,Ci]
+    y = torch.empty((B, H, W, Co), dtype=x.dtype, device="cuda")
+    d = dpp.dpp_conv_desc(B, H, W, Ci, Co, P, CODES[x.dtype], int(first_layer))
+    dpp.dpp_conv3x3(d, x, stale, wd, cuda(bias), y, stream=stream)
+    return y
+
+
+# ------------------------------------------------------------ groupnorm
+def gn_desc(x, G, eps, P):
+    B, H, W, C = x.shape
+    return dpp.dpp_gn_desc(B, H, W, C, G, P, eps, CODES[x.dtype])
+
+
+def groupnorm(x, stats_prev, G, eps, gamma, beta, P, y=None, stream=None):
+    """Returns (y, stats_next) as device tensors."""
+    x = cuda(x)
+    d = gn_desc(x, G, eps, P)
+    B = x.shape[0]
+    stats_next = torch.empty((P, B, G, 2), dtype=torch.float32, device="cuda")
+    nws = dpp.dpp_groupnorm_workspace_bytes(d)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    if y is None:
+        y = torch.empty_like(x)
+    dpp.dpp_groupnorm(d, x, cuda(stats_prev) if stats_prev is not None else None, stats_next,
+                      cuda(gamma), cuda(beta), y, ws, nws, stream=stream)
+    return y, stats_next
+
+
+# ------------------------------------------------------------ attention
+def attn_desc(x, H, W, heads, P, n_ctx=0, c_ctx=0):
+    B, N, C = x.shape
+    assert N == H * W
+    return dpp.dpp_attn_desc(B, H, W, C, heads, C // heads, P, n_ctx, c_ctx, CODES[x.dtype])
+
+
+def self_attn(x, wts, kv_prev, H, W, heads, P, stream=None):
+    """Returns (y, kv_next) as device tensors."""
+    x = cuda(x)
+    B, N, C = x.shape
+    d = attn_desc(x, H, W, heads, P)
+    kv_next = torch.empty((B, N, 2, C), dtype=x.dtype, device="cuda")
+    y = torch.empty_like(x)
+    nws = dpp.dpp_self_attn_workspace_bytes(d)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    w = {k: cuda(v) for k, v in wts.items()}
+    dpp.dpp_self_attn(d, x, w["wq"], w["wk"], w["wv"], w["wo"], kv_prev, kv_next, y, ws, nws,
+                      stream=stream)
+    return y, kv_next
+
+
+def cross_attn(x, ctx, wts, H, W, heads, stream=None):
+    x = cuda(x)
+    ctx = cuda(ctx)
+    d = attn_desc(x, H, W, heads, 1, ctx.shape[1], ctx.shape[2])
+    y = torch.empty_like(x)
+    nws = dpp.dpp_cross_attn_workspace_bytes(d)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    w = {k: cuda(v) for k, v in wts.items()}
+    dpp.dpp_cross_attn(d, x, ctx, w["wq"], w["wk"], w["wv"], w["wo"], y, ws, nws, stream=stream)
+    return y
+
+
+# ------------------------------------------------------------------ CFG
+def cfg(u, c, scale, out=None, ws=None):
+    u, c = cuda(u), cuda(c)
+    n = u.numel()
+    if out is None:
+        out = torch.empty_like(u)
+    sums = torch.zeros(3, dtype=torch.float64, device="cuda")
+    nws = dpp.dpp_cfg_workspace_bytes(n)
+    if ws is None:
+        ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    dpp.dpp_cfg_combine(u, c, scale, n, out, sums, ws, nws)
+    return out, sums, ws

@@ -1,0 +1,176 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/dpp.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run on a machine without a device).
+
+The pointers below are fake, 16-byte-aligned addresses: every call here must
+fail validation, which never dereferences them.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import displaced_patch_parallelism_02_b300 as dpp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dpp.h")
+
+A = 0x7f0000000000  # fake device addresses, far apart
+Bp = 0x7f1000000000
+Cp = 0x7f2000000000
+Dp = 0x7f3000000000
+Ep = 0x7f4000000000
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dpp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls_and_helpers():
+    names = declared_functions()
+    for n in ["dpp_conv3x3", "dpp_groupnorm", "dpp_self_attn", "dpp_cfg_combine",
+              "dpp_refresh_stale", "dpp_cross_attn", "dpp_status_string", "dpp_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(dpp.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_has_every_declared_name():
+    missing = [n for n in declared_functions() if not callable(getattr(dpp, n, None))]
+    assert not missing, missing
+
+
+def test_status_strings_and_version():
+    assert dpp.dpp_status_string(dpp.DPP_OK) == "DPP_OK"
+    assert dpp.dpp_status_string(dpp.DPP_ERR_ALIAS) == "DPP_ERR_ALIAS"
+    assert dpp.dpp_status_string(99) == "DPP_ERR_UNKNOWN"
+    assert dpp.dpp_version() >= 100
+
+
+def conv(**kw):
+    d = dict(B=1, H=8, W=8, C_in=16, C_out=16, P=2, dtype=dpp.DPP_BF16, first_layer=0)
+    d.update(kw)
+    return dpp.dpp_conv_desc(**d)
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(H=9), {}, dpp.DPP_ERR_INVALID_ARG),             # H % P != 0
+    (dict(C_in=12), {}, dpp.DPP_ERR_INVALID_ARG),         # bf16 needs C % 8 == 0
+    (dict(P=0), {}, dpp.DPP_ERR_INVALID_ARG),
+    (dict(dtype=5), {}, dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(x=0), dpp.DPP_ERR_INVALID_ARG),             # null input
+    ({}, dict(x=A + 8), dpp.DPP_ERR_ALIGN),
+    ({}, dict(y=A + 64), dpp.DPP_ERR_ALIAS),              # output overlaps input
+    ({}, dict(y=Bp + 32), dpp.DPP_ERR_ALIAS),             # output overlaps stale
+])
+def test_conv_validation(kw, ptrs, want):
+    p = dict(x=A, stale=Bp, w=Cp, bias=None, y=Dp)
+    p.update(ptrs)
+    st = dpp.dpp_conv3x3(conv(**kw), p["x"], p["stale"], p["w"], p["bias"], p["y"],
+                         stream=0, raise_on_error=False)
+    assert st == want
+
+
+def gn(**kw):
+    d = dict(B=1, H=8, W=8, C=32, G=4, P=2, eps=1e-5, dtype=dpp.DPP_BF16)
+    d.update(kw)
+    return dpp.dpp_gn_desc(**d)
+
+
+def test_gn_workspace_query_is_pure_and_positive():
+    assert dpp.dpp_groupnorm_workspace_bytes(gn()) > 0
+    assert dpp.dpp_groupnorm_workspace_bytes(gn(C=30)) == 0  # invalid desc
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(C=30), {}, dpp.DPP_ERR_INVALID_ARG),            # C % G
+    (dict(H=7), {}, dpp.DPP_ERR_INVALID_ARG),             # H % P
+    ({}, dict(ws=0), dpp.DPP_ERR_WORKSPACE),
+    ({}, dict(ws_bytes=16), dpp.DPP_ERR_WORKSPACE),
+    ({}, dict(stats_prev=Ep + 16), dpp.DPP_ERR_ALIAS),    # prev overlaps next
+    ({}, dict(gamma=Cp), dpp.DPP_ERR_INVALID_ARG),        # gamma without beta
+    ({}, dict(y=A + 32), dpp.DPP_ERR_ALIAS),              # partial in-place overlap
+    ({}, dict(stats_next=0), dpp.DPP_ERR_INVALID_ARG),
+])
+def test_gn_validation(kw, ptrs, want):
+    d = gn(**kw)
+    p = dict(x=A, stats_prev=None, stats_next=Ep, gamma=None, beta=None, y=Dp, ws=Bp,
+             ws_bytes=1 << 20)
+    p.update(ptrs)
+    st = dpp.dpp_groupnorm(d, p["x"], p["stats_prev"], p["stats_next"], p["gamma"], p["beta"],
+                           p["y"], p["ws"], p["ws_bytes"], stream=0, raise_on_error=False)
+    assert st == want
+
+
+def attn(**kw):
+    d = dict(B=1, H=8, W=8, C=128, heads=2, head_dim=64, P=2, n_ctx=0, c_ctx=0,
+             dtype=dpp.DPP_BF16)
+    d.update(kw)
+    return dpp.dpp_attn_desc(**d)
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(head_dim=32, C=64), {}, dpp.DPP_ERR_UNSUPPORTED),
+    (dict(C=192), {}, dpp.DPP_ERR_INVALID_ARG),           # C != heads * 64
+    (dict(H=9), {}, dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(kv_prev=Ep + 256), dpp.DPP_ERR_ALIAS),      # stale overlaps next
+    ({}, dict(ws=0), dpp.DPP_ERR_WORKSPACE),
+    ({}, dict(wq=0), dpp.DPP_ERR_INVALID_ARG),
+])
+def test_self_attn_validation(kw, ptrs, want):
+    d = attn(**kw)
+    p = dict(x=A, wq=Cp, wk=Cp + 65536, wv=Cp + 2 * 65536, wo=Cp + 3 * 65536, kv_prev=None,
+             kv_next=Ep, y=Dp, ws=Bp, ws_bytes=1 << 24)
+    p.update(ptrs)
+    st = dpp.dpp_self_attn(d, p["x"], p["wq"], p["wk"], p["wv"], p["wo"], p["kv_prev"],
+                           p["kv_next"], p["y"], p["ws"], p["ws_bytes"], stream=0,
+                           raise_on_error=False)
+    assert st == want
+
+
+def test_cross_attn_validation():
+    d = attn(n_ctx=0, c_ctx=0)
+    st = dpp.dpp_cross_attn(d, A, Bp, Cp, Cp, Cp, Cp, Dp, Ep, 1 << 24, stream=0,
+                            raise_on_error=False)
+    assert st == dpp.DPP_ERR_INVALID_ARG
+    d = attn(n_ctx=77, c_ctx=2048)
+    assert dpp.dpp_cross_attn_workspace_bytes(d) > 0
+    st = dpp.dpp_cross_attn(d, A, Bp, Cp, Cp, Cp, Cp, Dp, Ep, 16, stream=0, raise_on_error=False)
+    assert st == dpp.DPP_ERR_WORKSPACE
+
+
+def test_cfg_validation():
+    n = 1000
+    ws = dpp.dpp_cfg_workspace_bytes(n)
+    assert ws >= 16 + 3 * 8
+    assert dpp.dpp_cfg_combine(A, Bp, 7.5, n, Cp + 4, None, None, 0, stream=0,
+                               raise_on_error=False) == dpp.DPP_ERR_ALIGN
+    assert dpp.dpp_cfg_combine(A, Bp, 7.5, n, Cp, Dp, None, 0, stream=0,
+                               raise_on_error=False) == dpp.DPP_ERR_WORKSPACE
+    assert dpp.dpp_cfg_combine(A, Bp, 7.5, n, A + 16, None, None, 0, stream=0,
+                               raise_on_error=False) == dpp.DPP_ERR_ALIAS
+    assert dpp.dpp_cfg_combine(0, Bp, 7.5, n, Cp, None, None, 0, stream=0,
+                               raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+
+
+def test_refresh_validation():
+    f = dpp.dpp_refresh_stale
+    assert f(A, Bp, 1, 10, 64, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+    assert f(A, Bp, 1, 8, 40, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+    assert f(A, Bp, 1, 8, 64, 65, stream=0, raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+    assert f(A, A + 64, 1, 8, 64, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_ALIAS
+    assert f(A + 8, Bp, 1, 8, 64, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_ALIGN
+    # an empty mask is a valid no-op that launches nothing
+    assert f(A, Bp, 1, 8, 64, 4, patch_mask=0, stream=0, raise_on_error=False) == dpp.DPP_OK
+
+
+def test_error_raises_with_status_name():
+    with pytest.raises(dpp.DppError, match="DPP_ERR_INVALID_ARG"):
+        dpp.dpp_conv3x3(conv(H=9), A, Bp, Cp, None, Dp, stream=0)

@@ -1,0 +1,149 @@
+"""GPU parity on the SDXL-shaped workloads at full size, in the launch
+configuration the benchmark times.
+
+Where the fp64 oracle would take minutes, it evaluates a seeded sample of the
+outputs: for the conv, the first and last row of every band (the rows that
+read the stale halo) plus one interior row; for attention, the first and last
+query of every sampled band plus random queries; for GroupNorm, a subset of
+bands (each band's statistics still cover its whole composite image).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests import gpu_ops as G
+
+pytestmark = pytest.mark.gpu
+BF16 = torch.bfloat16
+RNG = np.random.default_rng(2024)
+
+
+def halo_rows(H, P, extra=1):
+    rows = []
+    Hp = H // P
+    for p in range(P):
+        lo, hi = p * Hp, (p + 1) * Hp
+        rows += [lo, hi - 1]
+        if Hp > 2:
+            rows += list(RNG.integers(lo + 1, hi - 1, size=extra))
+    return sorted(set(int(r) for r in rows))
+
+
+def band_queries(N, P, bands, n_random=32):
+    Np = N // P
+    qs = []
+    for p in bands:
+        qs += [p * Np, (p + 1) * Np - 1] + list(RNG.integers(p * Np, (p + 1) * Np, size=n_random))
+    return np.array(sorted(set(int(q) for q in qs)))
+
+
+def test_sdxl_1024_conv_groupnorm_four_displaced_steps(cuda_device):
+    w = wl.WORKLOADS["sdxl_1024_conv"]
+    c = w.conv
+    shape = (c.B, c.H, c.W, c.C)
+    Fs = wl.activation_steps(shape, w.index, w.displaced_steps, w.stale_scale, w.dtype)
+    Wt = wl.conv_weight(c.C, c.C, wl.seed_of(w.index, 0, wl.T_CONV_W), w.dtype)
+    gamma, beta = wl.gn_affine(c.C, w.index)
+    W64, g64, b64 = G.f64(Wt), G.f64(gamma), G.f64(beta)
+
+    stale = torch.empty(shape, dtype=BF16, device="cuda")
+    row_bytes = c.W * c.C * 2
+    y = G.conv(Fs[0], None, Wt, None, c.P)                            # step 0: synchronous
+    _, stats = G.groupnorm(y, None, w.groups, w.eps, gamma, beta, c.P)
+    G.dpp.dpp_refresh_stale(G.cuda(Fs[0]), stale, c.B, c.H, row_bytes, c.P)
+    Y_prev = oracle.conv3x3(G.f64(Fs[0]), W64)
+    for s in range(1, w.displaced_steps + 1):
+        Fd = G.cuda(Fs[s])
+        y = G.conv(Fd, stale, Wt, None, c.P)
+        g, stats = G.groupnorm(y, stats, w.groups, w.eps, gamma, beta, c.P)
+        G.dpp.dpp_refresh_stale(Fd, stale, c.B, c.H, row_bytes, c.P)
+        Y = oracle.displaced_conv3x3(G.f64(Fs[s]), G.f64(Fs[s - 1]), W64, None, c.P)
+        G.assert_rms_close(G.f64(y), Y, G.TOL[BF16], f"conv step {s}")
+        GN = oracle.displaced_groupnorm(Y, Y_prev, w.groups, w.eps, g64, b64, c.P)
+        G.assert_rms_close(G.f64(g), GN, G.TOL[BF16], f"groupnorm step {s}")
+        Y_prev = Y
+    torch.cuda.synchronize()
+    assert torch.equal(stale.cpu(), Fs[-1])  # the refreshed buffer is the last fresh input
+
+
+def _attn_case(w, bands=None, n_random=32):
+    a = w.attn
+    F = wl.normal((a.B, a.N, a.C), wl.seed_of(w.index, 0, wl.T_ATTN_X), dtype=w.dtype)
+    S = wl.perturbed(F, wl.seed_of(w.index, 1, wl.T_ATTN_X), w.stale_scale)
+    wts = wl.attn_weights(a, w.index, w.dtype)
+    _, kv_s = G.self_attn(S, wts, None, a.H, a.W, a.heads, a.P)
+    y, kv_f = G.self_attn(F, wts, kv_s, a.H, a.W, a.heads, a.P)
+    w64 = {k: G.f64(v) for k, v in wts.items()}
+    qs = None if bands is None else band_queries(a.N, a.P, bands, n_random)
+    ref = oracle.displaced_self_attention(G.f64(F), G.f64(S), w64["wq"], w64["wk"], w64["wv"],
+                                          w64["wo"], a.heads, a.P, queries=qs)
+    got = G.f64(y) if qs is None else G.f64(y)[:, qs]
+    G.assert_rms_close(got, ref, G.TOL[BF16], f"{w.name} self-attn")
+    # fresh K/V published for the next step: sampled tokens
+    toks = band_queries(a.N, a.P, range(a.P), 8)
+    kv_ref = oracle.kv_state(G.f64(F[:, toks]), w64["wk"], w64["wv"])
+    G.assert_rms_close(G.f64(kv_f[:, toks]), kv_ref, G.TOL[BF16], f"{w.name} kv_next")
+    return F
+
+
+def test_sdxl_1024_attn_self_and_cross(cuda_device):
+    w = wl.WORKLOADS["sdxl_1024_attn"]
+    a = w.attn
+    F = _attn_case(w)
+    ctx = wl.context(a, w.index, w.dtype)
+    wts = wl.cross_weights(a, w.index, w.dtype)
+    y = G.cross_attn(F, ctx, wts, a.H, a.W, a.heads)
+    w64 = {k: G.f64(v) for k, v in wts.items()}
+    ref = oracle.cross_attention(G.f64(F), G.f64(ctx), w64["wq"], w64["wk"], w64["wv"],
+                                 w64["wo"], a.heads)
+    G.assert_rms_close(G.f64(y), ref, G.TOL[BF16], "cross-attn")
+
+
+def _conv_gn_case(w, gn_bands):
+    c = w.conv
+    shape = (c.B, c.H, c.W, c.C)
+    F = wl.normal(shape, wl.seed_of(w.index, 0, wl.T_FRESH), dtype=w.dtype)
+    S = wl.perturbed(F, wl.seed_of(w.index, 1, wl.T_STALE_NOISE), w.stale_scale)
+    Wt = wl.conv_weight(c.C, c.C, wl.seed_of(w.index, 0, wl.T_CONV_W), w.dtype)
+    y = G.conv(F, S, Wt, None, c.P)
+    rows = halo_rows(c.H, c.P)
+    ref = oracle.displaced_conv3x3(G.f64(F), G.f64(S), G.f64(Wt), None, c.P, out_rows=rows)
+    G.assert_rms_close(G.f64(y[:, rows]), ref, G.TOL[BF16], f"{w.name} conv")
+    del y
+    # GroupNorm on the same tensors: stale state from a synchronous call on S
+    gamma, beta = wl.gn_affine(c.C, w.index)
+    _, st = G.groupnorm(S, None, w.groups, w.eps, gamma, beta, c.P)
+    g, _ = G.groupnorm(F, st, w.groups, w.eps, gamma, beta, c.P)
+    GN = oracle.displaced_groupnorm(G.f64(F), G.f64(S), w.groups, w.eps, G.f64(gamma),
+                                    G.f64(beta), c.P, bands=gn_bands)
+    Hp = c.H // c.P
+    sel = np.concatenate([np.arange(p * Hp, (p + 1) * Hp) for p in gn_bands])
+    G.assert_rms_close(G.f64(g[:, sel]), GN[:, sel], G.TOL[BF16], f"{w.name} groupnorm")
+
+
+def test_sdxl_2048_conv_groupnorm(cuda_device):
+    _conv_gn_case(wl.WORKLOADS["sdxl_2048"], gn_bands=range(8))
+
+
+def test_sdxl_2048_self_attn(cuda_device):
+    _attn_case(wl.WORKLOADS["sdxl_2048"], bands=range(8), n_random=16)
+
+
+def test_sdxl_3840_conv_groupnorm(cuda_device):
+    _conv_gn_case(wl.WORKLOADS["sdxl_3840_cfg"], gn_bands=[0, 3, 7])
+
+
+def test_sdxl_3840_self_attn(cuda_device):
+    _attn_case(wl.WORKLOADS["sdxl_3840_cfg"], bands=[0, 7], n_random=24)
+
+
+def test_sdxl_3840_cfg_combine(cuda_device):
+    w = wl.WORKLOADS["sdxl_3840_cfg"]
+    u, c = wl.guidance_maps(w.cfg_shape, w.index)
+    out, sums, _ = G.cfg(u, c, w.cfg_scale)
+    ref_out, ref_sums = oracle.cfg_combine(G.f64(u), G.f64(c), w.cfg_scale)
+    G.assert_rms_close(G.f64(out), ref_out, 1e-4, "cfg out")
+    np.testing.assert_allclose(sums.cpu().numpy(), ref_sums, rtol=1e-5)
+    assert abs(sums[0].item() / sums[1].item() - oracle.rel_mae(ref_sums)) < 1e-5
