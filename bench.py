@@ -197,7 +197,8 @@ class Step:
         self.sa_ws = torch.empty(self.sa_ws_n, dtype=torch.uint8, device=dev)
         self.xa_ws_n = dpp.dpp_cross_attn_workspace_bytes(self.cross_desc)
         self.xa_ws = torch.empty(self.xa_ws_n, dtype=torch.uint8, device=dev)
-        self.kv = [torch.empty((a.B, a.N, 2, a.C), dtype=bf, device=dev) for _ in range(2)]
+        self.kv = [torch.empty((a.B, a.N, 2, a.C), dtype=torch.float16, device=dev)
+                   for _ in range(2)]  # fp16 K/V state of a bf16 attention layer
         self.ya = torch.empty((a.B, a.N, a.C), dtype=bf, device=dev)
         self.yc = torch.empty((a.B, a.N, a.C), dtype=bf, device=dev)
         # guidance maps
@@ -414,6 +415,9 @@ def main():
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
     core = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(K)]
+    for a_, b_ in core:  # create the CUDA events now; the library re-records them
+        a_.record(s)
+        b_.record(s)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()

@@ -238,13 +238,13 @@ dpp_status dpp_conv3x3(const dpp_conv_desc *d, const void *x, const void *stale_
 // ---------------------------------------------------------------- attention
 size_t dpp_self_attn_workspace_bytes(const dpp_attn_desc *d) {
   if (check_attn(d, false) != DPP_OK) return 0;
-  const size_t n = attn_tokens(*d) * d->C * elem_size(d->dtype);
+  const size_t n = attn_tokens(*d) * d->C * elem_bytes(inter_elem(d->dtype));
   return 2 * align_up(n, 256);  // Q, O
 }
 
 size_t dpp_cross_attn_workspace_bytes(const dpp_attn_desc *d) {
   if (check_attn(d, true) != DPP_OK) return 0;
-  const size_t es = elem_size(d->dtype);
+  const size_t es = elem_bytes(inter_elem(d->dtype));
   const size_t n = attn_tokens(*d) * d->C * es;
   const size_t kv = (size_t)d->B * d->n_ctx * 2 * d->C * es;
   return 2 * align_up(n, 256) + align_up(kv, 256);  // Q, O, context K/V
@@ -263,8 +263,10 @@ dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, 
   const size_t need = dpp_self_attn_workspace_bytes(d);
   if (!ws || ws_bytes < need) return DPP_ERR_WORKSPACE;
   const size_t es = elem_size(d->dtype);
+  const Elem te = inter_elem(d->dtype), tl = layer_elem(d->dtype);
   const size_t nt = attn_tokens(*d);
-  const size_t nx = nt * d->C * es, nkv = nt * 2 * d->C * es;
+  const size_t nx = nt * d->C * es, nkv = nt * 2 * d->C * elem_bytes(te);
+  const size_t nq = nt * d->C * elem_bytes(te);
   if (overlap(kv_prev, nkv, kv_next, nkv)) return DPP_ERR_ALIAS;
   if (overlap(y, nx, kv_next, nkv) || overlap(y, nx, kv_prev, nkv) || overlap(ws, need, y, nx) ||
       overlap(ws, need, x, nx) || overlap(ws, need, kv_next, nkv) ||
@@ -274,20 +276,19 @@ dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, 
   cudaStream_t s = (cudaStream_t)stream;
   char *wsb = reinterpret_cast<char *>(ws);
   void *q = wsb;
-  void *o = wsb + align_up(nx, 256);
+  void *o = wsb + align_up(nq, 256);
   const int C = d->C;
   const int M = (int)nt;
   // 1. Q for every token (every band's own queries), fresh K/V into kv_next
-  GemmArgs qkv{x, {wq, wk, wv}, C, M, 3 * C, C, q, C, C, kv_next, 2 * C, d->dtype};
+  GemmArgs qkv{x, {wq, wk, wv}, C, M, 3 * C, C, q, C, C, kv_next, 2 * C, tl, tl, te};
   cudaError_t e = counted(launch_gemm_simt(qkv, s), 1);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 2. displaced attention core
-  AttnArgs a{q, kv_next, kv_prev, o, d->B, d->H * d->W, d->H * d->W, C, d->heads, d->P,
-             d->dtype};
+  AttnArgs a{q, kv_next, kv_prev, o, d->B, d->H * d->W, d->H * d->W, C, d->heads, d->P, te};
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 3. output projection
-  GemmArgs op{o, {wo, nullptr, nullptr}, C, M, C, C, y, C, C, nullptr, 0, d->dtype};
+  GemmArgs op{o, {wo, nullptr, nullptr}, C, M, C, C, y, C, C, nullptr, 0, te, tl, tl};
   return from_cuda(counted(launch_gemm_simt(op, s), 1));
 }
 
@@ -303,8 +304,10 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
   const size_t need = dpp_cross_attn_workspace_bytes(d);
   if (!ws || ws_bytes < need) return DPP_ERR_WORKSPACE;
   const size_t es = elem_size(d->dtype);
+  const Elem te = inter_elem(d->dtype), tl = layer_elem(d->dtype);
   const size_t nt = attn_tokens(*d);
   const size_t nx = nt * d->C * es;
+  const size_t nq = nt * d->C * elem_bytes(te);
   if (overlap(ws, need, y, nx) || overlap(ws, need, x, nx) ||
       overlap(ws, need, ctx, (size_t)d->B * d->n_ctx * d->c_ctx * es))
     return DPP_ERR_ALIAS;
@@ -312,20 +315,20 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
   cudaStream_t s = (cudaStream_t)stream;
   char *wsb = reinterpret_cast<char *>(ws);
   void *q = wsb;
-  void *o = wsb + align_up(nx, 256);
-  void *kv = wsb + 2 * align_up(nx, 256);
+  void *o = wsb + align_up(nq, 256);
+  void *kv = wsb + 2 * align_up(nq, 256);
   const int C = d->C;
-  GemmArgs qg{x, {wq, nullptr, nullptr}, C, (int)nt, C, C, q, C, C, nullptr, 0, d->dtype};
+  GemmArgs qg{x, {wq, nullptr, nullptr}, C, (int)nt, C, C, q, C, C, nullptr, 0, tl, tl, te};
   cudaError_t e = counted(launch_gemm_simt(qg, s), 1);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   GemmArgs kvg{ctx, {wk, wv, nullptr}, C, d->B * d->n_ctx, 2 * C, d->c_ctx,
-               kv, 2 * C, 2 * C, nullptr, 0, d->dtype};
+               kv, 2 * C, 2 * C, nullptr, 0, tl, tl, te};
   e = counted(launch_gemm_simt(kvg, s), 1);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
-  AttnArgs a{q, kv, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, d->dtype};
+  AttnArgs a{q, kv, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, te};
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
-  GemmArgs op{o, {wo, nullptr, nullptr}, C, (int)nt, C, C, y, C, C, nullptr, 0, d->dtype};
+  GemmArgs op{o, {wo, nullptr, nullptr}, C, (int)nt, C, C, y, C, C, nullptr, 0, te, tl, tl};
   return from_cuda(counted(launch_gemm_simt(op, s), 1));
 }
 

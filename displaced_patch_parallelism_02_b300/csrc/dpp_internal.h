@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -54,20 +55,30 @@ cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *st
                            const void *w, const float *bias, void *y, int *status,
                            cudaStream_t s);
 
+// Element types inside the library.  Attention layers whose activations are
+// bf16 keep Q, O and the K/V state in fp16: the same tensor-core rate with
+// an 11-bit significand, which keeps the chained roundings of the layer
+// within the bf16 error budget (bf16 intermediates alone exceed it).
+enum Elem : int { E_F32 = 0, E_BF16 = 1, E_F16 = 2 };
+
+inline Elem layer_elem(dpp_dtype t) { return t == DPP_BF16 ? E_BF16 : E_F32; }
+inline Elem inter_elem(dpp_dtype t) { return t == DPP_BF16 ? E_F16 : E_F32; }
+inline size_t elem_bytes(Elem e) { return e == E_F32 ? 4 : 2; }
+
 // GEMM D = A * B^T with B given as up to 3 row blocks (weights [out, in]);
 // output columns [0, split) go to out0 (leading dim ld0), the rest to out1
 // (leading dim ld1, column index minus split).
 struct GemmArgs {
-  const void *A;      // [M, K]
-  const void *B[3];   // each [b_rows, K]
+  const void *A;      // [M, K], element type ta
+  const void *B[3];   // each [b_rows, K], element type tb
   int b_rows;         // rows per B block
   int M, N, K;
-  void *out0;
+  void *out0;         // element type to
   int ld0;
   int split;
   void *out1;
   int ld1;
-  dpp_dtype dtype;
+  Elem ta, tb, to;
 };
 cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s);
@@ -76,13 +87,14 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s);
 // q: [B, Nq, C]; kv_fresh / kv_stale: [B, Nkv, 2, C] (kv_stale may be null:
 // everything fresh).  Query band p (of P) attends over fresh keys of its own
 // band and stale keys elsewhere; with Nkv != Nq (cross attention) P must be 1.
+// q, kv and o share the element type `te` (fp16 or fp32).
 struct AttnArgs {
   const void *q;
   const void *kv_fresh;
   const void *kv_stale;
   void *o;
   int B, Nq, Nkv, C, heads, P;
-  dpp_dtype dtype;
+  Elem te;
 };
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s);

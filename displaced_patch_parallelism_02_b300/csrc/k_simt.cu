@@ -36,6 +36,14 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, flo
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
+template <>
+__device__ __forceinline__ void load4<__half>(const __half *p, float f[4]) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(p);
+  const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+  const float2 a = __half22float2(h[0]), b = __half22float2(h[1]);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
 template <typename T>
 __device__ __forceinline__ T from_f(float v);
 template <>
@@ -44,6 +52,8 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
+template <>
+__device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
 
 constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
 
@@ -117,24 +127,24 @@ conv_simt_kernel(const T *__restrict__ x, const T *__restrict__ stale, const T *
 }
 
 // ----------------------------------------------------------------- gemm
-template <typename T>
+template <typename TA, typename TB, typename TO>
 __global__ void __launch_bounds__(NT) gemm_simt_kernel(const __grid_constant__ GemmArgs g) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
-  const T *A = reinterpret_cast<const T *>(g.A);
+  const TA *A = reinterpret_cast<const TA *>(g.A);
   const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
   const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
   const int lm = tid / 4, lq = tid % 4;
   const int am = m0 + lm, bn = n0 + lm;
-  const T *arow = A + (size_t)(am < g.M ? am : 0) * g.K;
-  const T *brow = reinterpret_cast<const T *>(g.B[bn < g.N ? bn / g.b_rows : 0]) +
-                  (size_t)(bn < g.N ? bn % g.b_rows : 0) * g.K;
+  const TA *arow = A + (size_t)(am < g.M ? am : 0) * g.K;
+  const TB *brow = reinterpret_cast<const TB *>(g.B[bn < g.N ? bn / g.b_rows : 0]) +
+                   (size_t)(bn < g.N ? bn % g.b_rows : 0) * g.K;
   float acc[4][4] = {};
   for (int k0 = 0; k0 < g.K; k0 += BK) {
     const int kk = k0 + lq * 4;
     float a4[4] = {0.f, 0.f, 0.f, 0.f}, b4[4] = {0.f, 0.f, 0.f, 0.f};
-    if (am < g.M && kk < g.K) load4<T>(arow + kk, a4);
-    if (bn < g.N && kk < g.K) load4<T>(brow + kk, b4);
+    if (am < g.M && kk < g.K) load4<TA>(arow + kk, a4);
+    if (bn < g.N && kk < g.K) load4<TB>(brow + kk, b4);
     __syncthreads();
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -155,8 +165,8 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const __grid_constant__ G
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
     }
   }
-  T *o0 = reinterpret_cast<T *>(g.out0);
-  T *o1 = reinterpret_cast<T *>(g.out1);
+  TO *o0 = reinterpret_cast<TO *>(g.out0);
+  TO *o1 = reinterpret_cast<TO *>(g.out1);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int mm = m0 + ty + 16 * i;
@@ -166,9 +176,9 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const __grid_constant__ G
       const int nn = n0 + tx + 16 * j;
       if (nn >= g.N) continue;
       if (nn < g.split)
-        o0[(size_t)mm * g.ld0 + nn] = from_f<T>(acc[i][j]);
+        o0[(size_t)mm * g.ld0 + nn] = from_f<TO>(acc[i][j]);
       else
-        o1[(size_t)mm * g.ld1 + (nn - g.split)] = from_f<T>(acc[i][j]);
+        o1[(size_t)mm * g.ld1 + (nn - g.split)] = from_f<TO>(acc[i][j]);
     }
   }
 }
@@ -328,10 +338,14 @@ cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *
 
 cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s) {
   dim3 grid((unsigned)((g.M + BM - 1) / BM), (unsigned)((g.N + BN - 1) / BN));
-  if (g.dtype == DPP_BF16)
-    gemm_simt_kernel<__nv_bfloat16><<<grid, NT, 0, s>>>(g);
+  if (g.ta == E_F32 && g.tb == E_F32 && g.to == E_F32)
+    gemm_simt_kernel<float, float, float><<<grid, NT, 0, s>>>(g);
+  else if (g.ta == E_BF16 && g.tb == E_BF16 && g.to == E_F16)
+    gemm_simt_kernel<__nv_bfloat16, __nv_bfloat16, __half><<<grid, NT, 0, s>>>(g);
+  else if (g.ta == E_F16 && g.tb == E_BF16 && g.to == E_BF16)
+    gemm_simt_kernel<__half, __nv_bfloat16, __nv_bfloat16><<<grid, NT, 0, s>>>(g);
   else
-    gemm_simt_kernel<float><<<grid, NT, 0, s>>>(g);
+    return cudaErrorNotSupported;
   return cudaGetLastError();
 }
 
@@ -340,10 +354,10 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s) {
   const int tpb = (Np + AQ - 1) / AQ;
   dim3 grid((unsigned)(tpb * a.P), (unsigned)a.heads, (unsigned)a.B);
   const size_t smem = kAttnSmemFloats * sizeof(float);
-  if (a.dtype == DPP_BF16) {
-    cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attn_simt_kernel<__nv_bfloat16><<<grid, NT, smem, s>>>(a);
+  if (a.te == E_F16) {
+    cudaFuncSetAttribute(attn_simt_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    attn_simt_kernel<__half><<<grid, NT, smem, s>>>(a);
   } else {
     cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);

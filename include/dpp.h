@@ -36,7 +36,11 @@
  *     layer belongs to head c / head_dim.
  *   - Types: DPP_BF16 = bf16 storage, fp32 accumulation and softmax;
  *     DPP_F32 = fp32 storage and arithmetic (SIMT path, no TF32).
- *     Biases, GroupNorm affine and statistics are always fp32.
+ *     Biases, GroupNorm affine and statistics are always fp32.  Attention
+ *     layers of type DPP_BF16 keep their K/V state (and their internal Q
+ *     and O) in fp16: same tensor-core rate as bf16 with an 11-bit
+ *     significand, which keeps the layer's chained roundings inside the
+ *     bf16 error bound; bf16 intermediates alone exceed it.
  *   - Streams: every call is asynchronous on `stream` (a cudaStream_t;
  *     NULL = legacy default stream).
  *   - Errors: argument checks run on the host before anything is launched
@@ -154,8 +158,9 @@ size_t dpp_groupnorm_workspace_bytes(const dpp_gn_desc *desc);
  *   x, y     : [B, N, C] tokens, desc->dtype.
  *   wq..wo   : [C, C] torch Linear [out, in], desc->dtype, no bias.
  *   kv_prev  : [B, N, 2, C] (K then V per token) from the previous step,
- *              or NULL for the synchronous step.
- *   kv_next  : [B, N, 2, C] output; must not overlap kv_prev.
+ *              or NULL for the synchronous step.  fp16 for DPP_BF16
+ *              layers, fp32 for DPP_F32 layers.
+ *   kv_next  : [B, N, 2, C] output, same type; must not overlap kv_prev.
  *   ws       : dpp_self_attn_workspace_bytes(desc) bytes (Q and O).
  * Requires head_dim == 64, H % P == 0, C == heads * 64.
  * ------------------------------------------------------------------------- */

@@ -10,11 +10,18 @@ import torch
 import displaced_patch_parallelism_02_b300 as dpp
 
 CODES = {torch.float32: dpp.DPP_F32, torch.bfloat16: dpp.DPP_BF16}
+KV_DTYPE = {torch.float32: torch.float32, torch.bfloat16: torch.float16}  # attention state
 TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}  # max-abs error / RMS of the output
 
 
 def cuda(t):
     return None if t is None else t.contiguous().to("cuda")
+
+
+def to_storage(a, dtype):
+    """Rounds an fp64 array to a tensor's storage type (RNE) and back: the
+    value a layer of that type stores for the next one to read."""
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).to(torch.float64).numpy()
 
 
 def f64(t):
@@ -79,7 +86,7 @@ def self_attn(x, wts, kv_prev, H, W, heads, P, stream=None):
     x = cuda(x)
     B, N, C = x.shape
     d = attn_desc(x, H, W, heads, P)
-    kv_next = torch.empty((B, N, 2, C), dtype=x.dtype, device="cuda")
+    kv_next = torch.empty((B, N, 2, C), dtype=KV_DTYPE[x.dtype], device="cuda")
     y = torch.empty_like(x)
     nws = dpp.dpp_self_attn_workspace_bytes(d)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")

@@ -174,3 +174,14 @@ def test_refresh_validation():
 def test_error_raises_with_status_name():
     with pytest.raises(dpp.DppError, match="DPP_ERR_INVALID_ARG"):
         dpp.dpp_conv3x3(conv(H=9), A, Bp, Cp, None, Dp, stream=0)
+
+
+def test_rejected_calls_launch_nothing():
+    before = dpp.dpp_launch_count()
+    dpp.dpp_conv3x3(conv(H=9), A, Bp, Cp, None, Dp, stream=0, raise_on_error=False)
+    dpp.dpp_groupnorm(gn(C=30), A, None, Ep, None, None, Dp, Bp, 1 << 20, stream=0,
+                      raise_on_error=False)
+    dpp.dpp_self_attn(attn(H=9), A, Cp, Cp, Cp, Cp, None, Ep, Dp, Bp, 1 << 24, stream=0,
+                      raise_on_error=False)
+    dpp.dpp_refresh_stale(A, A + 64, 1, 8, 64, 4, stream=0, raise_on_error=False)
+    assert dpp.dpp_launch_count() == before
