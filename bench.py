@@ -57,11 +57,12 @@ def work_model(w):
     conv = 2.0 * c.B * c.H * c.W * c.C * 9 * c.C
     core = 4.0 * a.B * a.N * a.N * a.head_dim * a.heads
     proj = 2.0 * a.B * a.N * a.C * 3 * a.C + 2.0 * a.B * a.N * a.C * a.C
-    xq_o = 2.0 * 2.0 * a.B * a.N * a.C * a.C
+    cross = a.n_ctx > 0
+    xq_o = 2.0 * 2.0 * a.B * a.N * a.C * a.C if cross else 0.0
     xkv = 2.0 * a.B * a.n_ctx * a.c_ctx * 2 * a.C
     xcore = 4.0 * a.B * a.N * a.n_ctx * a.head_dim * a.heads
     act_bytes = c.B * c.H * c.W * c.C * 2
-    n_cfg = int(np.prod(w.cfg_shape))
+    n_cfg = int(np.prod(w.cfg_shape)) if w.cfg_shape else 0
     return {
         "conv_flop": conv, "self_core_flop": core, "self_proj_flop": proj,
         "cross_flop": xq_o + xkv + xcore, "cross_core_flop": xcore,
@@ -185,8 +186,10 @@ class Step:
         xs = put(Xs)
         del X, Xs
         self.aw = {k: put(v) for k, v in wl.attn_weights(a, w.index, w.dtype).items()}
-        self.xw = {k: put(v) for k, v in wl.cross_weights(a, w.index, w.dtype).items()}
-        ctx = wl.context(a, w.index, w.dtype)
+        self.cross = a.n_ctx > 0
+        self.xw = ({k: put(v) for k, v in wl.cross_weights(a, w.index, w.dtype).items()}
+                   if self.cross else {})
+        ctx = wl.context(a, w.index, w.dtype) if self.cross else torch.zeros(16)
         self.host_ctx = ctx.pin_memory()
         self.ctx = put(ctx)
         self.attn_desc = dpp.dpp_attn_desc(a.B, a.H, a.W, a.C, a.heads, a.head_dim, a.P, 0, 0,
@@ -195,14 +198,15 @@ class Step:
                                             a.n_ctx, a.c_ctx, dpp.DPP_BF16)
         self.sa_ws_n = dpp.dpp_self_attn_workspace_bytes(self.attn_desc)
         self.sa_ws = torch.empty(self.sa_ws_n, dtype=torch.uint8, device=dev)
-        self.xa_ws_n = dpp.dpp_cross_attn_workspace_bytes(self.cross_desc)
-        self.xa_ws = torch.empty(self.xa_ws_n, dtype=torch.uint8, device=dev)
+        self.xa_ws_n = dpp.dpp_cross_attn_workspace_bytes(self.cross_desc) if self.cross else 0
+        self.xa_ws = torch.empty(max(self.xa_ws_n, 16), dtype=torch.uint8, device=dev)
         self.kv = [torch.empty((a.B, a.N, 2, a.C), dtype=torch.float16, device=dev)
                    for _ in range(2)]  # fp16 K/V state of a bf16 attention layer
         self.ya = torch.empty((a.B, a.N, a.C), dtype=bf, device=dev)
         self.yc = torch.empty((a.B, a.N, a.C), dtype=bf, device=dev)
         # guidance maps
-        u, cc = wl.guidance_maps(w.cfg_shape, w.index)
+        self.has_cfg = w.cfg_shape is not None
+        u, cc = wl.guidance_maps(w.cfg_shape or (4,), w.index)
         self.host_u, self.host_c = u.pin_memory(), cc.pin_memory()
         self.u, self.c = put(u), put(cc)
         self.n_cfg = u.numel()
@@ -245,12 +249,14 @@ class Step:
         if core_events:
             dpp.dpp_set_attn_core_events(None, None)
         rec(3)
-        dpp.dpp_cross_attn(self.cross_desc, self.ya, self.ctx, self.xw["wq"], self.xw["wk"],
-                           self.xw["wv"], self.xw["wo"], self.yc, self.xa_ws, self.xa_ws_n,
-                           stream=s)
+        if self.cross:
+            dpp.dpp_cross_attn(self.cross_desc, self.ya, self.ctx, self.xw["wq"],
+                               self.xw["wk"], self.xw["wv"], self.xw["wo"], self.yc, self.xa_ws,
+                               self.xa_ws_n, stream=s)
         rec(4)
-        dpp.dpp_cfg_combine(self.u, self.c, w.cfg_scale, self.n_cfg, self.cfg_out, self.sums,
-                            self.cfg_ws, self.cfg_ws_n, stream=s)
+        if self.has_cfg:
+            dpp.dpp_cfg_combine(self.u, self.c, w.cfg_scale, self.n_cfg, self.cfg_out,
+                                self.sums, self.cfg_ws, self.cfg_ws_n, stream=s)
         rec(5)
         dpp.dpp_refresh_stale(self.x, self.stale, c.B, c.H, self.row_bytes, c.P, stream=s)
         rec(6)
@@ -370,7 +376,7 @@ def run_reference(args, w, ws, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "step_tflop_full": model["step_flop"] / 1e12},
+        "config": {"workload": w.name, "step_tflop_full": model["step_flop"] / 1e12},
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -387,8 +393,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=["sdxl_3840_cfg", "sdxl_2048"],
+                    help="sdxl_2048 (no guidance maps or text context) is the smaller case "
+                         "used for profiler captures")
     args = ap.parse_args()
-    w = wl.WORKLOADS[WORKLOAD]
+    w = wl.WORKLOADS[args.workload]
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, w, ws, rank)
@@ -446,8 +455,8 @@ def main():
     op_ms = {op: sum(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(K)) / K
              for j, op in enumerate(step.ops)}
     core_ms = sum(a.elapsed_time(b) for a, b in core) / K
-    tf = lambda f, ms: f / (ms / 1e3) / 1e12
-    gb = lambda b, ms: b / (ms / 1e3) / 1e9
+    tf = lambda f, ms: f / (ms / 1e3) / 1e12 if f and ms > 0 else None
+    gb = lambda b, ms: b / (ms / 1e3) / 1e9 if b and ms > 0 else None
     sus = peaks["bf16_tflops_sustained"]
     ops = {
         "conv": {"ms": op_ms["conv"], "tflops": tf(model["conv_flop"], op_ms["conv"])},
@@ -462,9 +471,9 @@ def main():
         "refresh": {"ms": op_ms["refresh"], "gbs": gb(model["refresh_bytes"], op_ms["refresh"])},
     }
     for k, v in ops.items():
-        if "tflops" in v:
+        if v.get("tflops") is not None:
             v["frac_of_sustained_bf16"] = v["tflops"] / sus
-        else:
+        elif v.get("gbs") is not None:
             v["frac_of_hbm"] = v["gbs"] / peaks["hbm_gbs"]
 
     # end to end: pinned host inputs -> device, step, results -> host
@@ -502,9 +511,12 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
-            "config": {"workload": WORKLOAD, "latent": [2, 480, 480, 320], "bands": 8,
-                       "attn_tokens": [2, 57600], "attn_channels": 640, "heads": 10,
-                       "text_ctx": [77, 2048], "cfg_maps": [2, 4, 480, 480],
+            "config": {"workload": w.name,
+                       "latent": [w.conv.B, w.conv.H, w.conv.W, w.conv.C], "bands": w.conv.P,
+                       "attn_tokens": [w.attn.B, w.attn.N], "attn_channels": w.attn.C,
+                       "heads": w.attn.heads,
+                       "text_ctx": [w.attn.n_ctx, w.attn.c_ctx] if w.attn.n_ctx else None,
+                       "cfg_maps": [2] + list(w.cfg_shape) if w.cfg_shape else None,
                        "parallelism": f"replicas{ws}",
                        "l2": "no flush: inputs and step working set exceed the 126 MB L2"},
             "roofline": {"kernel": "self-attention core", "bound": "tensor",
