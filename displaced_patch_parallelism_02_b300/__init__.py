@@ -71,6 +71,8 @@ _SIGNATURES = {
     "dpp_groupnorm": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _sz, _vp]),
     "dpp_groupnorm_workspace_bytes": (_sz, [ctypes.POINTER(dpp_gn_desc)]),
+    "dpp_groupnorm_static": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                   _vp]),
     "dpp_self_attn": (_st, [ctypes.POINTER(dpp_attn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _vp, _sz, _vp]),
     "dpp_self_attn_workspace_bytes": (_sz, [ctypes.POINTER(dpp_attn_desc)]),
@@ -159,6 +161,19 @@ def dpp_groupnorm(desc: dpp_gn_desc, x, stats_prev, stats_next, gamma, beta, y, 
                                     _ptr(stats_next), _ptr(gamma), _ptr(beta), _ptr(y),
                                     _ptr(ws), int(ws_bytes), _stream(stream)),
                   "dpp_groupnorm", raise_on_error)
+
+
+DPP_GN_STATIC_SCRATCH_BYTES = 1 << 20
+
+
+def dpp_groupnorm_static(desc: dpp_gn_desc, x, stats_prev, stats_next, gamma, beta, y,
+                         stream=None, raise_on_error: bool = True) -> int:
+    """dpp_groupnorm with its scratch in the library's static device array
+    (for callers that cannot allocate; see include/dpp.h)."""
+    return _check(lib.dpp_groupnorm_static(ctypes.byref(desc), _ptr(x), _ptr(stats_prev),
+                                           _ptr(stats_next), _ptr(gamma), _ptr(beta), _ptr(y),
+                                           _stream(stream)),
+                  "dpp_groupnorm_static", raise_on_error)
 
 
 def dpp_self_attn_workspace_bytes(desc: dpp_attn_desc) -> int:

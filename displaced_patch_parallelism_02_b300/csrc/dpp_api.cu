@@ -226,6 +226,26 @@ dpp_status dpp_groupnorm(const dpp_gn_desc *d, const void *x, const float *stats
                                             (cudaStream_t)stream), 2));
 }
 
+dpp_status dpp_groupnorm_static(const dpp_gn_desc *d, const void *x, const float *stats_prev,
+                                float *stats_next, const float *gamma, const float *beta,
+                                void *y, dpp_stream stream) {
+  dpp_status st = check_gn(d);
+  if (st != DPP_OK) return st;
+  if (!x || !y || !stats_next) return DPP_ERR_INVALID_ARG;
+  if ((gamma == nullptr) != (beta == nullptr)) return DPP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(stats_next) ||
+      (stats_prev && !aligned16(stats_prev)))
+    return DPP_ERR_ALIGN;
+  if (gn_workspace(*d) > kGnStaticScratchBytes) return DPP_ERR_WORKSPACE;
+  const size_t nx = (size_t)d->B * d->H * d->W * d->C * elem_size(d->dtype);
+  const size_t ns = (size_t)d->P * d->B * d->G * 2 * sizeof(float);
+  if (y != x && overlap(y, nx, x, nx)) return DPP_ERR_ALIAS;
+  if (overlap(stats_prev, ns, stats_next, ns) || overlap(stats_next, ns, y, nx))
+    return DPP_ERR_ALIAS;
+  return from_cuda(counted(launch_groupnorm_static(*d, x, stats_prev, stats_next, gamma, beta,
+                                                   y, (cudaStream_t)stream), 2));
+}
+
 // --------------------------------------------------------------------- conv
 dpp_status dpp_conv3x3(const dpp_conv_desc *d, const void *x, const void *stale_prev,
                        const void *w, const float *bias, void *y, dpp_stream stream) {

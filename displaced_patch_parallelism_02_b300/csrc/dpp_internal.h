@@ -45,6 +45,13 @@ cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *s
                              float *stats_next, const float *gamma, const float *beta,
                              void *y, void *ws, cudaStream_t s);
 
+// GroupNorm with its scratch in a static device array of this many bytes
+// (no workspace argument, no allocation).
+constexpr size_t kGnStaticScratchBytes = DPP_GN_STATIC_SCRATCH_BYTES;
+cudaError_t launch_groupnorm_static(const dpp_gn_desc &d, const void *x, const float *stats_prev,
+                                    float *stats_next, const float *gamma, const float *beta,
+                                    void *y, cudaStream_t s);
+
 // SIMT implicit-GEMM conv (fp32 / bf16 storage, fp32 math)
 cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *stale,
                              const void *w, const float *bias, void *y, cudaStream_t s);

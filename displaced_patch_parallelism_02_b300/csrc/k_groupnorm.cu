@@ -17,6 +17,8 @@
 //      scale and shift per channel and normalises its chunk.  Pass 2
 //      re-reads the chunk pass 1 just read; it comes from L2 when the
 //      tensor fits there.
+#include <mutex>
+
 #include "dpp_internal.h"
 
 namespace dpp {
@@ -250,6 +252,52 @@ cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *s
                                                          gamma, beta, d.eps);
   }
   return cudaGetLastError();
+}
+
+}  // namespace dpp
+
+// ---------------------------------------------------------------------------
+// Allocation-free GroupNorm.  Some callers cannot allocate device memory:
+// plugins that run inside a host program which owns the whole device-memory
+// budget (an inference server's pre-planned arena, a framework layer API
+// that hands out no workspace), or code that must not call cudaMalloc on a
+// hot path because cudaMalloc may synchronise the device.  For them the
+// partial-sum scratch lives in this file-scope device array instead of a
+// caller workspace.  Every GPU that loads the library holds the array until
+// the process exits.  All calls share it: calls whose kernels overlap on the
+// GPU (two streams, or two host threads) race on it.
+namespace dpp {
+
+static __device__ __align__(256) unsigned char g_gn_static_scratch[kGnStaticScratchBytes];
+
+namespace {
+std::mutex g_gn_static_mutex;
+void *g_gn_static_ptr[64] = {};
+}  // namespace
+
+cudaError_t launch_groupnorm_static(const dpp_gn_desc &d, const void *x, const float *stats_prev,
+                                    float *stats_next, const float *gamma, const float *beta,
+                                    void *y, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void *scratch = nullptr;
+  {
+    // Set-up, once per device, with that device current: the host-side name
+    // of the array is not a device address, so look the address up.
+    std::lock_guard<std::mutex> lock(g_gn_static_mutex);
+    if (!g_gn_static_ptr[dev]) {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_gn_static_scratch);
+      if (e != cudaSuccess) return e;
+      g_gn_static_ptr[dev] = p;
+    }
+    scratch = g_gn_static_ptr[dev];
+  }
+  // The partial sums are fully written by the first pass before the second
+  // reads them, so nothing in the array needs clearing between calls.
+  return launch_groupnorm(d, x, stats_prev, stats_next, gamma, beta, y, scratch, s);
 }
 
 }  // namespace dpp

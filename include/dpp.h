@@ -148,6 +148,33 @@ dpp_status dpp_groupnorm(const dpp_gn_desc *desc, const void *x, const float *st
 size_t dpp_groupnorm_workspace_bytes(const dpp_gn_desc *desc);
 
 /* ---------------------------------------------------------------------------
+ * dpp_groupnorm_static -- dpp_groupnorm without a workspace argument.  The
+ * pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory -- plugins running inside a host program that owns
+ * the whole device-memory budget (an inference server's pre-planned arena, a
+ * framework layer API that hands out no workspace), or code that must not
+ * call cudaMalloc on a hot path because it may synchronise the device.
+ * Arguments and results are those of dpp_groupnorm; its scratch lives in a
+ * static device array of DPP_GN_STATIC_SCRATCH_BYTES that every GPU loading
+ * the library holds until the process exits.  It allocates nothing.
+ *   - Returns DPP_ERR_WORKSPACE when dpp_groupnorm_workspace_bytes(desc)
+ *     exceeds DPP_GN_STATIC_SCRATCH_BYTES (with G = 32 groups that needs
+ *     about 4000 band x chunk units, far beyond any latent this library's
+ *     partitioning produces).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents:
+ *     calls whose kernels overlap on the GPU (several streams or host
+ *     threads) race on it.
+ * ------------------------------------------------------------------------- */
+#define DPP_GN_STATIC_SCRATCH_BYTES (1u << 20)
+dpp_status dpp_groupnorm_static(const dpp_gn_desc *desc, const void *x,
+                                const float *stats_prev, float *stats_next,
+                                const float *gamma, const float *beta, void *y,
+                                dpp_stream stream);
+
+/* ---------------------------------------------------------------------------
  * dpp_self_attn -- DistriSelfAttentionPP (section 注意力机制拆分 of the
  * DistriFusion developer guide, attn1).  For band p:
  *   Q = x[band p] wq^T;  K/V rows of band p's tokens are x[band p] wk^T /

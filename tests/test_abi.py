@@ -185,3 +185,15 @@ def test_rejected_calls_launch_nothing():
                       raise_on_error=False)
     dpp.dpp_refresh_stale(A, A + 64, 1, 8, 64, 4, stream=0, raise_on_error=False)
     assert dpp.dpp_launch_count() == before
+
+
+def test_static_groupnorm_rejects_oversize_scratch_on_the_host():
+    # 8192 groups of one channel over a 256x256 latent need ~38 MB of partials
+    big = gn(H=256, W=256, C=8192, G=8192, P=1)
+    assert dpp.dpp_groupnorm_workspace_bytes(big) > dpp.DPP_GN_STATIC_SCRATCH_BYTES
+    before = dpp.dpp_launch_count()
+    st = dpp.dpp_groupnorm_static(big, A, None, Ep, None, None, Dp, stream=0,
+                                  raise_on_error=False)
+    assert st == dpp.DPP_ERR_WORKSPACE and dpp.dpp_launch_count() == before
+    assert dpp.dpp_groupnorm_static(gn(C=30), A, None, Ep, None, None, Dp, stream=0,
+                                    raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
