@@ -113,6 +113,37 @@ cudaError_t counted(cudaError_t e, int kernels) {
   return e;
 }
 
+// Projection GEMM: the tcgen05 kernel when the shape and types allow it
+// (16-bit operands), the SIMT kernel otherwise (fp32 layers).
+cudaError_t gemm(const GemmArgs &g, cudaStream_t s) {
+  if (gemm_tc_supported(g)) return counted(launch_gemm_tc(g, device_status_ptr(), s), 1);
+  return counted(launch_gemm_simt(g, s), 1);
+}
+
+// Bytes of the fp16 copy of Wo a bf16 attention layer keeps in its workspace
+// (the output projection's two operands must share one 16-bit type).
+size_t wo16_bytes(const dpp_attn_desc &d) {
+  return d.dtype == DPP_BF16 ? align_up((size_t)d.C * d.C * 2, 256) : 0;
+}
+
+// Output projection y = O wo^T; for bf16 layers wo is first cast to fp16
+// into `wo16` so both operands are fp16.
+cudaError_t out_proj(const dpp_attn_desc &d, const void *o, const void *wo, void *wo16, void *y,
+                     int M, cudaStream_t s) {
+  const Elem te = inter_elem(d.dtype), tl = layer_elem(d.dtype);
+  const int C = d.C;
+  const void *w = wo;
+  Elem tw = tl;
+  if (d.dtype == DPP_BF16) {
+    cudaError_t e = counted(launch_cast_bf16_f16(wo, wo16, (size_t)C * C, s), 1);
+    if (e != cudaSuccess) return e;
+    w = wo16;
+    tw = E_F16;
+  }
+  GemmArgs op{o, {w, nullptr, nullptr}, C, M, C, C, y, C, C, nullptr, 0, te, tw, tl};
+  return gemm(op, s);
+}
+
 // Launches the attention core, bracketed by the profiling events when set.
 cudaError_t attn_core(const AttnArgs &a, cudaStream_t s) {
   if (g_core_start && g_core_stop) cudaEventRecord(g_core_start, s);
@@ -259,7 +290,7 @@ dpp_status dpp_conv3x3(const dpp_conv_desc *d, const void *x, const void *stale_
 size_t dpp_self_attn_workspace_bytes(const dpp_attn_desc *d) {
   if (check_attn(d, false) != DPP_OK) return 0;
   const size_t n = attn_tokens(*d) * d->C * elem_bytes(inter_elem(d->dtype));
-  return 2 * align_up(n, 256);  // Q, O
+  return 2 * align_up(n, 256) + wo16_bytes(*d);  // Q, O, fp16 Wo
 }
 
 size_t dpp_cross_attn_workspace_bytes(const dpp_attn_desc *d) {
@@ -267,7 +298,7 @@ size_t dpp_cross_attn_workspace_bytes(const dpp_attn_desc *d) {
   const size_t es = elem_bytes(inter_elem(d->dtype));
   const size_t n = attn_tokens(*d) * d->C * es;
   const size_t kv = (size_t)d->B * d->n_ctx * 2 * d->C * es;
-  return 2 * align_up(n, 256) + align_up(kv, 256);  // Q, O, context K/V
+  return 2 * align_up(n, 256) + align_up(kv, 256) + wo16_bytes(*d);  // Q, O, ctx K/V, Wo
 }
 
 dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, const void *wk,
@@ -301,15 +332,14 @@ dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, 
   const int M = (int)nt;
   // 1. Q for every token (every band's own queries), fresh K/V into kv_next
   GemmArgs qkv{x, {wq, wk, wv}, C, M, 3 * C, C, q, C, C, kv_next, 2 * C, tl, tl, te};
-  cudaError_t e = counted(launch_gemm_simt(qkv, s), 1);
+  cudaError_t e = gemm(qkv, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 2. displaced attention core
   AttnArgs a{q, kv_next, kv_prev, o, d->B, d->H * d->W, d->H * d->W, C, d->heads, d->P, te};
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 3. output projection
-  GemmArgs op{o, {wo, nullptr, nullptr}, C, M, C, C, y, C, C, nullptr, 0, te, tl, tl};
-  return from_cuda(counted(launch_gemm_simt(op, s), 1));
+  return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256), y, M, s));
 }
 
 dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx, const void *wq,
@@ -339,17 +369,18 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
   void *kv = wsb + 2 * align_up(nq, 256);
   const int C = d->C;
   GemmArgs qg{x, {wq, nullptr, nullptr}, C, (int)nt, C, C, q, C, C, nullptr, 0, tl, tl, te};
-  cudaError_t e = counted(launch_gemm_simt(qg, s), 1);
+  cudaError_t e = gemm(qg, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   GemmArgs kvg{ctx, {wk, wv, nullptr}, C, d->B * d->n_ctx, 2 * C, d->c_ctx,
                kv, 2 * C, 2 * C, nullptr, 0, tl, tl, te};
-  e = counted(launch_gemm_simt(kvg, s), 1);
+  e = gemm(kvg, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   AttnArgs a{q, kv, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, te};
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
-  GemmArgs op{o, {wo, nullptr, nullptr}, C, (int)nt, C, C, y, C, C, nullptr, 0, te, tl, tl};
-  return from_cuda(counted(launch_gemm_simt(op, s), 1));
+  const size_t nkvb = (size_t)d->B * d->n_ctx * 2 * d->C * elem_bytes(te);
+  return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256) + align_up(nkvb, 256), y,
+                            (int)nt, s));
 }
 
 }  // extern "C"

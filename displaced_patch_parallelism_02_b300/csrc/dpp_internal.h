@@ -89,6 +89,9 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s);
+bool gemm_tc_supported(const GemmArgs &g);
+// bf16 -> fp16 element copy (weights feeding an fp16 tensor-core operand)
+cudaError_t launch_cast_bf16_f16(const void *in, void *out, size_t n, cudaStream_t s);
 
 // attention core: O = softmax(Q K^T / 8) V for head_dim 64.
 // q: [B, Nq, C]; kv_fresh / kv_stale: [B, Nkv, 2, C] (kv_stale may be null:

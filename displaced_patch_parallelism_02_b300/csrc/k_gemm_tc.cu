@@ -1,0 +1,317 @@
+// Tensor-core GEMM for the attention projections: D = A * B^T on tcgen05.
+//
+// A [M, K] and the weight blocks B_i [b_rows, K] are K-major 16-bit tensors
+// (both fp16 or both bf16).  The output columns are split between two
+// destinations: the QKV projection writes Q to the workspace and the fresh
+// K/V of every token straight into the next step's attention state (the
+// refresh of DistriSelfAttentionPP's state costs no extra pass).
+//
+// Persistent, warp-specialised, one CTA per SM:
+//   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 per stage
+//               (B as BN/64 boxes of 64 rows, each from the weight block that
+//               holds it), 128-byte swizzle, STAGES-deep mbarrier ring;
+//   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
+//               (M = 128, N = BN, K = 16 per instruction), fp32 accumulators
+//               double-buffered in TMEM (2 x BN columns);
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, convert, store.
+// Tiles are ordered n-fastest so CTAs running together share A rows in L2.
+#include "tc_common.cuh"
+
+namespace dpp {
+
+namespace tc {
+
+bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base,
+                  const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                  CUtensorMapSwizzle swizzle) {
+  using Fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                          const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                          const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                          CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Fn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return false;
+    fn = reinterpret_cast<Fn>(p);
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, type, (cuuint32_t)rank, const_cast<void *>(base),
+            reinterpret_cast<const cuuint64_t *>(dims),
+            reinterpret_cast<const cuuint64_t *>(strides),
+            reinterpret_cast<const cuuint32_t *>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+namespace {
+
+using namespace tc;
+
+struct GemmTcParams {
+  int M, N, K, b_rows;
+  void *out0;
+  int ld0, split;
+  void *out1;
+  int ld1;
+  int out_f16;  // 1: fp16 output, 0: bf16 output
+  int m_tiles, n_tiles;
+  int *status;
+};
+
+constexpr int kThreads = 192;
+constexpr int BM = 128, BK = 64;
+
+template <int BN, int STAGES, bool IN_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+               const GemmTcParams p) {
+  constexpr uint32_t A_BYTES = BM * BK * 2;
+  constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  constexpr uint32_t IDESC = idesc_f16(BM, BN, IN_BF16);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;  // MMA completion on the abort path
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB0);
+    prefetch_tmap(&tmB1);
+    prefetch_tmap(&tmB2);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int KB = (p.K + BK - 1) / BK;
+  const int tiles = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;  // per-stage bits, for the abort drain
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
+          uint8_t *sa = smem + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) {
+            const int n = n0 + 64 * j;
+            int mat = n / p.b_rows;
+            if (mat > 2) mat = 2;
+            const CUtensorMap *mp = mat == 0 ? &tmB0 : (mat == 1 ? &tmB1 : &tmB2);
+            tma_load_2d(sa + A_BYTES + j * 64 * 128, mp, &full[stage], kb * BK,
+                        n - mat * p.b_rows);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag)  // let copies already in flight land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if ((armed >> s) & 1u) mbar_drain(&full[s], (armed_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // --------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t ad = desc_sw128_kmajor(sa);
+          const uint64_t bd = desc_sw128_kmajor(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16_ss(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0);
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+      }
+      if (*abort_flag) {  // no MMA may still be writing TMEM when it is freed
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else {  // ------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
+      const int m = m0 + row;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
+        tmem_wait_ld();
+        const int n = n0 + c * 32;
+        if (m < p.M && n < p.N) {
+          uint4 *dst;
+          if (n < p.split)
+            dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out0) +
+                                            (size_t)m * p.ld0 + n);
+          else
+            dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out1) +
+                                            (size_t)m * p.ld1 + (n - p.split));
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = __uint_as_float(r[v * 8 + 2 * e]);
+              const float b = __uint_as_float(r[v * 8 + 2 * e + 1]);
+              ow[e] = p.out_f16 ? pack_half2(a, b) : pack_bf162(a, b);
+            }
+            dst[v] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int BN, int STAGES, bool IN_BF16>
+cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
+  const CUtensorMapDataType ty = tma_type(g.ta);
+  CUtensorMap ma, mb[3];
+  {
+    const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.M};
+    const uint64_t str[1] = {(uint64_t)g.K * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tiled(&ma, ty, 2, g.A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  for (int i = 0; i < 3; ++i) {
+    const void *b = g.B[i] ? g.B[i] : g.B[0];
+    const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.b_rows};
+    const uint64_t str[1] = {(uint64_t)g.K * 2};
+    const uint32_t box[2] = {64, 64};
+    if (!encode_tiled(&mb[i], ty, 2, b, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  GemmTcParams p{g.M, g.N, g.K, g.b_rows, g.out0, g.ld0, g.split, g.out1, g.ld1,
+                 g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, (g.N + BN - 1) / BN, status};
+  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512;
+  auto k = gemm_tc_kernel<BN, STAGES, IN_BF16>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int grid = tiles < sms ? tiles : sms;
+  k<<<grid, kThreads, smem, s>>>(ma, mb[0], mb[1], mb[2], p);
+  return cudaGetLastError();
+}
+
+__global__ void cast_bf16_f16_kernel(const __nv_bfloat16 *__restrict__ in, __half *__restrict__ out,
+                                     size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    out[i] = __float2half_rn(__bfloat162float(in[i]));
+}
+
+}  // namespace
+
+cudaError_t launch_cast_bf16_f16(const void *in, void *out, size_t n, cudaStream_t s) {
+  size_t blocks = (n + 255) / 256;
+  if (blocks > 1184) blocks = 1184;
+  if (blocks < 1) blocks = 1;
+  cast_bf16_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>((const __nv_bfloat16 *)in,
+                                                        (__half *)out, n);
+  return cudaGetLastError();
+}
+
+bool gemm_tc_supported(const GemmArgs &g) {
+  const bool in16 = (g.ta == E_BF16 || g.ta == E_F16) && g.ta == g.tb;
+  const bool out16 = g.to == E_BF16 || g.to == E_F16;
+  return in16 && out16 && g.K % 8 == 0 && g.b_rows % 64 == 0 && g.N % 32 == 0 &&
+         g.split % 32 == 0 && g.ld0 % 8 == 0 && (g.out1 == nullptr || g.ld1 % 8 == 0) &&
+         (g.N + g.b_rows - 1) / g.b_rows <= 3 && g.M > 0;
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s) {
+  if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
+  const bool bf = g.ta == E_BF16;
+  if (g.N % 192 == 0)
+    return bf ? run<192, 5, true>(g, status, s) : run<192, 5, false>(g, status, s);
+  if (g.N % 256 == 0)
+    return bf ? run<256, 4, true>(g, status, s) : run<256, 4, false>(g, status, s);
+  return bf ? run<128, 6, true>(g, status, s) : run<128, 6, false>(g, status, s);
+}
+
+}  // namespace dpp

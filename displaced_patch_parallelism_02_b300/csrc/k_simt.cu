@@ -344,6 +344,8 @@ cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s) {
     gemm_simt_kernel<__nv_bfloat16, __nv_bfloat16, __half><<<grid, NT, 0, s>>>(g);
   else if (g.ta == E_F16 && g.tb == E_BF16 && g.to == E_BF16)
     gemm_simt_kernel<__half, __nv_bfloat16, __nv_bfloat16><<<grid, NT, 0, s>>>(g);
+  else if (g.ta == E_F16 && g.tb == E_F16 && g.to == E_BF16)
+    gemm_simt_kernel<__half, __half, __nv_bfloat16><<<grid, NT, 0, s>>>(g);
   else
     return cudaErrorNotSupported;
   return cudaGetLastError();
