@@ -108,6 +108,7 @@ struct AttnArgs {
 };
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s);
+bool attn_tc_supported(const AttnArgs &a);
 
 // device status word (bounded waits record DPP_ERR_TIMEOUT here)
 int *device_status_ptr();

@@ -1,0 +1,395 @@
+// Displaced attention core on tcgen05 (DistriSelfAttentionPP, section
+// 注意力机制拆分 of the DistriFusion developer guide): a band's queries attend
+// over the fresh K/V of their own band and the stale K/V of every other band.
+// Also serves cross-attention (one fresh segment, the text context).
+//
+// O = softmax(Q K^T / 8) V per (batch, head, band), head_dim 64, fp16 Q/K/V/P,
+// fp32 accumulators and softmax.  One CTA handles two 128-query tiles of one
+// band so that one tile's softmax overlaps the other tile's MMAs:
+//   warp 0        TMA producer: both Q tiles once, then K and V tiles of 128
+//                 keys into 3-deep rings (128-byte swizzle).  The key range is
+//                 walked segment by segment -- own band from the fresh state,
+//                 the keys before and after it from the stale state -- so each
+//                 tile has one source; a segment's ragged last tile is aligned
+//                 to end at the segment end (masking its leading columns), so
+//                 no tile reads outside its segment when the segment holds at
+//                 least 128 keys.
+//   warp 1        TMEM owner and single-thread MMA issuer:
+//                   S_t = Q_t K^T   (M 128, N 128, K 64) into TMEM,
+//                   O_t += P_t V    (M 128, N 64, K 128) with P_t in shared
+//                                   memory (K-major) and V used MN-major.
+//   warps 4..7    softmax of query tile 0, warps 8..11 of tile 1: one thread
+//                 per query row (= TMEM lane); masked row max, p = 2^(s - m),
+//                 P written as fp16 in the 128-byte-swizzled layout, running
+//                 sum; the reference max m only moves when a row max exceeds
+//                 it by 8 (in log2 units), so the O accumulator in TMEM is
+//                 rarely rescaled; final O / l stored as fp16.
+#include "tc_common.cuh"
+
+namespace dpp {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 384;
+constexpr int KS = 3, VS = 3;  // K and V ring depths
+constexpr uint32_t TILE_BYTES = 128 * 128;  // 128 rows x 64 fp16
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
+constexpr uint32_t OFF_P = OFF_V + VS * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_P + 2 * 2 * TILE_BYTES;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+constexpr float kRescaleThreshold = 8.f;
+
+struct AttnTcParams {
+  int B, Nq, Nkv, C, P;
+  int has_stale;
+  int tpb;  // CTAs per band (two query tiles each)
+  void *o;
+  int *status;
+  float scale_log2;
+};
+
+struct KvTile {
+  int kv0, vlo, vhi, fresh;
+};
+
+struct Segs {
+  int lo[3], hi[3], fresh[3], ntiles[3], total;
+};
+
+__device__ __forceinline__ Segs make_segs(const AttnTcParams &p, int band) {
+  Segs s;
+  if (p.has_stale && p.Nkv == p.Nq) {
+    const int Np = p.Nq / p.P;
+    s.lo[0] = band * Np;  s.hi[0] = (band + 1) * Np; s.fresh[0] = 1;
+    s.lo[1] = 0;          s.hi[1] = band * Np;       s.fresh[1] = 0;
+    s.lo[2] = (band + 1) * Np; s.hi[2] = p.Nkv;      s.fresh[2] = 0;
+  } else {
+    s.lo[0] = 0; s.hi[0] = p.Nkv; s.fresh[0] = 1;
+    s.lo[1] = s.hi[1] = s.lo[2] = s.hi[2] = 0;
+    s.fresh[1] = s.fresh[2] = 0;
+  }
+  s.total = 0;
+  for (int i = 0; i < 3; ++i) {
+    const int L = s.hi[i] - s.lo[i];
+    s.ntiles[i] = L > 0 ? (L + 127) / 128 : 0;
+    s.total += s.ntiles[i];
+  }
+  return s;
+}
+
+__device__ __forceinline__ KvTile tile_of(const Segs &s, int j) {
+  int i = 0;
+  while (j >= s.ntiles[i]) {
+    j -= s.ntiles[i];
+    ++i;
+  }
+  const int lo = s.lo[i], hi = s.hi[i], L = hi - lo;
+  KvTile t;
+  t.fresh = s.fresh[i];
+  if (L < 128) {
+    t.kv0 = lo; t.vlo = 0; t.vhi = L;
+  } else if (j == s.ntiles[i] - 1 && (L & 127)) {
+    t.kv0 = hi - 128; t.vlo = lo + 128 * j - t.kv0; t.vhi = 128;
+  } else {
+    t.kv0 = lo + 128 * j; t.vlo = 0; t.vhi = 128;
+  }
+  return t;
+}
+
+// Warp-uniform bounded wait: every lane waits, then the warp agrees.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int *status) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmF,
+               const __grid_constant__ CUtensorMap tmS, const AttnTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  uint64_t *q_full = bars;
+  uint64_t *k_full = bars + 1, *k_empty = k_full + KS;
+  uint64_t *v_full = k_empty + KS, *v_empty = v_full + VS;
+  uint64_t *s_full = v_empty + VS, *s_empty = s_full + 2;
+  uint64_t *p_full = s_empty + 2, *p_empty = p_full + 2;
+  uint64_t *o_final = p_empty + 2, *drain = o_final + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int band = blockIdx.x / p.tpb, part = blockIdx.x % p.tpb;
+  const int head = blockIdx.y, b = blockIdx.z;
+  const int Np = p.Nq / p.P;
+  const int q0 = band * Np + part * 256;
+  const int qend = (band + 1) * Np;
+  const Segs segs = make_segs(p, band);
+  const int T = segs.total;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+    for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_empty[t], 128);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&p_empty[t], 1);
+      mbar_init(&o_final[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmF);
+    prefetch_tmap(&tmS);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------ producer
+      uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
+      mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
+      tma_load_2d(smem + OFF_Q, &tmQ, q_full, head * 64, b * p.Nq + q0);
+      tma_load_2d(smem + OFF_Q + TILE_BYTES, &tmQ, q_full, head * 64, b * p.Nq + q0 + 128);
+      for (int j = 0; j < T; ++j) {
+        const KvTile kt = tile_of(segs, j);
+        const CUtensorMap *m = kt.fresh ? &tmF : &tmS;
+        const int row = b * p.Nkv + kt.kv0;
+        const int ks = j % KS, vs = j % VS;
+        const uint32_t kph = (j / KS) & 1, vph = (j / VS) & 1;
+        if (!mbar_wait(&k_empty[ks], kph ^ 1u, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&k_full[ks], TILE_BYTES);
+        k_armed |= 1u << ks;
+        k_par = (k_par & ~(1u << ks)) | (kph << ks);
+        tma_load_2d(smem + OFF_K + ks * TILE_BYTES, m, &k_full[ks], head * 64, row);
+        if (!mbar_wait(&v_empty[vs], vph ^ 1u, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
+        v_armed |= 1u << vs;
+        v_par = (v_par & ~(1u << vs)) | (vph << vs);
+        tma_load_2d(smem + OFF_V + vs * TILE_BYTES, m, &v_full[vs], p.C + head * 64, row);
+      }
+      if (*abort_flag) {  // copies in flight must land before the CTA exits
+        mbar_drain(q_full, 0);
+        for (int i = 0; i < KS; ++i)
+          if ((k_armed >> i) & 1u) mbar_drain(&k_full[i], (k_par >> i) & 1u);
+        for (int i = 0; i < VS; ++i)
+          if ((v_armed >> i) & 1u) mbar_drain(&v_full[i], (v_par >> i) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------ MMA issuer
+      constexpr uint32_t IDESC_S = idesc_f16(128, 128, false);
+      constexpr uint32_t IDESC_O = idesc_f16(128, 64, false, true);
+      const uint32_t sQ = smem_u32(smem + OFF_Q), sK = smem_u32(smem + OFF_K);
+      const uint32_t sV = smem_u32(smem + OFF_V), sP = smem_u32(smem + OFF_P);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      auto qk = [&](int j, int t) -> bool {
+        if (!mbar_wait(&s_empty[t], (j & 1) ^ 1u, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint64_t ad = desc_sw128_kmajor(sQ + t * TILE_BYTES);
+        const uint64_t bd = desc_sw128_kmajor(sK + (j % KS) * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_f16_ss(tmem + t * 256, ad + 2 * k, bd + 2 * k, IDESC_S, k);
+        mma_commit(&s_full[t]);
+        return true;
+      };
+      auto pv = [&](int j, int t) -> bool {
+        if (!mbar_wait(&p_full[t], j & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t pb = sP + t * 2 * TILE_BYTES;
+        const uint32_t vb = sV + (j % VS) * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = desc_sw128_kmajor(pb + (kk >> 2) * TILE_BYTES) + 2 * (kk & 3);
+          const uint64_t bd = desc_sw128_mnmajor(vb + kk * 2048, 1024);
+          mma_f16_ss(tmem + t * 256 + 128, ad, bd, IDESC_O, (j | kk) != 0);
+        }
+        mma_commit(&p_empty[t]);
+        return true;
+      };
+      if (ok && T > 0) {
+        ok = mbar_wait(&k_full[0], 0, abort_flag, p.status) && qk(0, 0) && qk(0, 1);
+        if (ok) mma_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const bool next = j + 1 < T;
+        if (next) ok = mbar_wait(&k_full[(j + 1) % KS], ((j + 1) / KS) & 1, abort_flag, p.status);
+        ok = ok && mbar_wait(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status);
+        if (ok && next) ok = qk(j + 1, 0);
+        ok = ok && pv(j, 0);
+        if (ok && next) {
+          ok = qk(j + 1, 1);
+          if (ok) mma_commit(&k_empty[(j + 1) % KS]);
+        }
+        ok = ok && pv(j, 1);
+        if (ok) mma_commit(&v_empty[j % VS]);
+      }
+      if (ok) {
+        mma_commit(&o_final[0]);
+        mma_commit(&o_final[1]);
+      } else {  // nothing may still be writing TMEM when it is freed
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else if (warp >= 4) {  // --------------------------------------- softmax
+    const int t = (warp - 4) / 4;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 256, tO = tS + 128;
+    uint8_t *Pt = smem + OFF_P + t * 2 * TILE_BYTES;
+    const uint32_t swz = (uint32_t)(row & 7);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const KvTile kt = tile_of(segs, j);
+      if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t (&r)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32 * c]);
+        tmem_ld32(tS + 32 * c, r);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_empty[t]);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        const float v = (i >= kt.vlo && i < kt.vhi) ? __uint_as_float(sr[i]) * p.scale_log2
+                                                     : -INFINITY;
+        sr[i] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      float corr = 1.f;
+      if (mx > m_ref + kRescaleThreshold) {
+        corr = ex2_approx(m_ref - mx);  // 0 on the first tile
+        m_ref = mx;
+      }
+      l *= corr;
+      if (!warp_wait(&p_empty[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // rescale O (rare)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + 32 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+          tmem_st32(tO + 32 * c, r);
+        }
+        tmem_wait_st();
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {  // 16-byte chunk c holds keys 8c .. 8c+7
+        uint4 v;
+        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = ex2_approx(__uint_as_float(sr[8 * c + 2 * e]) - m_ref);
+          const float bb = ex2_approx(__uint_as_float(sr[8 * c + 2 * e + 1]) - m_ref);
+          sum += a + bb;
+          w[e] = pack_half2(a, bb);
+        }
+        *reinterpret_cast<uint4 *>(Pt + (c >> 3) * TILE_BYTES + row * 128 +
+                                   ((((uint32_t)c & 7u) ^ swz) << 4)) = v;
+      }
+      l += sum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+    if (ok && warp_wait(&o_final[t], 0, abort_flag, p.status)) {
+      tc_fence_after();
+      const int q = q0 + t * 128 + row;
+      const float inv = 1.f / l;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + 32 * c, r);
+        tmem_wait_ld();
+        if (q < qend) {
+          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(p.o) +
+                                                 ((size_t)b * p.Nq + q) * p.C + head * 64 + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              ow[e] = pack_half2(__uint_as_float(r[8 * v + 2 * e]) * inv,
+                                 __uint_as_float(r[8 * v + 2 * e + 1]) * inv);
+            dst[v] = o;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool attn_tc_supported(const AttnArgs &a) {
+  return a.te == E_F16 && a.C % 64 == 0 && a.heads * 64 == a.C && a.Nq % a.P == 0 &&
+         (a.P == 1 || a.Nkv == a.Nq) && a.Nkv > 0 && a.Nq > 0;
+}
+
+cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s) {
+  if (!attn_tc_supported(a)) return cudaErrorNotSupported;
+  CUtensorMap mq, mf, ms;
+  {
+    const uint64_t dims[2] = {(uint64_t)a.C, (uint64_t)a.B * a.Nq};
+    const uint64_t str[1] = {(uint64_t)a.C * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tiled(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.q, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  const uint64_t dims[2] = {(uint64_t)a.C * 2, (uint64_t)a.B * a.Nkv};
+  const uint64_t str[1] = {(uint64_t)a.C * 4};
+  const uint32_t box[2] = {64, 128};
+  if (!encode_tiled(&mf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.kv_fresh, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tiled(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    a.kv_stale ? a.kv_stale : a.kv_fresh, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const int Np = a.Nq / a.P;
+  AttnTcParams p{a.B, a.Nq, a.Nkv, a.C, a.P, a.kv_stale != nullptr ? 1 : 0,
+                 (Np + 255) / 256, a.o, status, 0.125f * 1.4426950408889634f};
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(a.P * p.tpb), (unsigned)a.heads, (unsigned)a.B);
+  attn_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(mq, mf, ms, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dpp
