@@ -283,8 +283,11 @@ dpp_status dpp_conv3x3(const dpp_conv_desc *d, const void *x, const void *stale_
                        const void *w, const float *bias, void *y, dpp_stream stream) {
   dpp_status st = check_conv(d, x, stale_prev, w, bias, y);
   if (st != DPP_OK) return st;
-  return from_cuda(
-      counted(launch_conv_simt(*d, x, stale_prev, w, bias, y, (cudaStream_t)stream), 1));
+  cudaStream_t s = (cudaStream_t)stream;
+  if (conv_tc_supported(*d))  // bf16: tensor cores; fp32: the SIMT kernel
+    return from_cuda(
+        counted(launch_conv_tc(*d, x, stale_prev, w, bias, y, device_status_ptr(), s), 1));
+  return from_cuda(counted(launch_conv_simt(*d, x, stale_prev, w, bias, y, s), 1));
 }
 
 // ---------------------------------------------------------------- attention

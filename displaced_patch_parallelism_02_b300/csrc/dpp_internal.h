@@ -58,6 +58,7 @@ cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *
 
 // tcgen05 implicit-GEMM conv (bf16); returns cudaErrorNotSupported when the
 // shape is outside what the kernel handles
+bool conv_tc_supported(const dpp_conv_desc &d);
 cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *stale,
                            const void *w, const float *bias, void *y, int *status,
                            cudaStream_t s);

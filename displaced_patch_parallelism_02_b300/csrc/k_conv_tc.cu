@@ -1,0 +1,311 @@
+// Displaced 3x3 conv (DistriConv2dPP, section 卷积层拆分 of the DistriFusion
+// developer guide) as an implicit GEMM on tcgen05.
+//
+//   Y[b,h,w,:] = bias + sum_{dy,dx} W_tap[:, :] . Z_p[b, h+dy-1, w+dx-1, :]
+//
+// GEMM view: M = output pixels, N = C_out, K = 9 taps x C_in.  An M tile is
+// 128 consecutive pixels of ONE image row (b, h, w0..w0+127), so for each tap
+// the A tile is a single TMA box of the input row h+dy-1 shifted by dx-1
+// pixels.  That row is either in the band that owns h (fresh input) or in a
+// neighbouring band (stale input, the halo); the producer picks the tensor
+// map per tap.  Rows -1 and H and columns -1 and W fall outside the tensor
+// and TMA fills them with zeros: the image padding costs nothing.
+//
+// Persistent, warp-specialised, one CTA per SM (the GEMM kernel's layout):
+//   warp 0      TMA producer: A box {64 ch, 128 px} from the fresh or stale
+//               map, B box {64 ch, 1 tap, BN out-ch} of the weights
+//               [C_out][3][3][C_in], 128-byte swizzle, STAGES-deep ring;
+//   warp 1      TMEM owner and single-thread tcgen05.mma issuer
+//               (M 128, N BN, K 16), two accumulators 256 columns apart;
+//   warps 2..5  epilogue: tcgen05.ld, + bias, bf16, 16-byte stores.
+#include "tc_common.cuh"
+
+namespace dpp {
+namespace {
+
+using namespace tc;
+
+struct ConvTcParams {
+  int B, H, W, Cin, Cout, P;
+  int nseg;      // 128-pixel segments per image row
+  int cblocks;   // 64-channel blocks of C_in
+  int m_tiles, n_tiles;
+  int use_stale; // 0: every input row comes from the fresh map
+  const float *bias;
+  __nv_bfloat16 *y;
+  int *status;
+};
+
+constexpr int kThreads = 192;
+constexpr int BM = 128, BK = 64;
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
+               const __grid_constant__ CUtensorMap tmW, const ConvTcParams p) {
+  constexpr uint32_t A_BYTES = BM * BK * 2;
+  constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t IDESC = idesc_f16(BM, BN, true);
+  static_assert(B_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmS);
+    prefetch_tmap(&tmW);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int KB = 9 * p.cblocks;
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int Hp = p.H / p.P;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        const int mt = t / p.n_tiles, n0 = (t % p.n_tiles) * BN;
+        const int seg = mt % p.nseg, rowid = mt / p.nseg;
+        const int h = rowid % p.H, b = rowid / p.H;
+        const int lo = (h / Hp) * Hp, hi = lo + Hp;
+        const int w0 = seg * BM;
+        for (int kb = 0; kb < KB; ++kb) {
+          const int tap = kb / p.cblocks, cb = kb - tap * p.cblocks;
+          const int hh = h + tap / 3 - 1, ww = w0 + tap % 3 - 1;
+          // rows outside [0, H) are zero-filled whichever map is used
+          const CUtensorMap *src = (p.use_stale && (hh < lo || hh >= hi)) ? &tmS : &tmX;
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
+          uint8_t *sa = smem + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          tma_load_4d(sa, src, &full[stage], cb * BK, ww, hh, b);
+          tma_load_3d(sa + A_BYTES, &tmW, &full[stage], cb * BK, tap, n0);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag)
+        for (int s = 0; s < STAGES; ++s)
+          if ((armed >> s) & 1u) mbar_drain(&full[s], (armed_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // --------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * 256;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t ad = desc_sw128_kmajor(sa);
+          const uint64_t bd = desc_sw128_kmajor(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16_ss(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0);
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+      }
+      if (*abort_flag) {
+        mma_commit(drain);
+        mbar_drain(drain, 0);
+      }
+    }
+  } else {  // ------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int px = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int mt = t / p.n_tiles, n0 = (t % p.n_tiles) * BN;
+      const int seg = mt % p.nseg, rowid = mt / p.nseg;  // rowid = b * H + h
+      const int w = seg * BM + px;
+      __nv_bfloat16 *yrow = p.y + ((size_t)rowid * p.W + w) * p.Cout;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, r);
+        tmem_wait_ld();
+        const int n = n0 + c * 32;
+        if (w < p.W && n < p.Cout) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int nv = n + 8 * v;
+            if (nv < p.Cout) {
+              float bv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) bv[e] = p.bias ? __ldg(p.bias + nv + e) : 0.f;
+              uint4 o;
+              uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                ow[e] = pack_bf162(__uint_as_float(r[8 * v + 2 * e]) + bv[2 * e],
+                                   __uint_as_float(r[8 * v + 2 * e + 1]) + bv[2 * e + 1]);
+              *reinterpret_cast<uint4 *>(yrow + nv) = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+constexpr size_t kSmemBudget = 227 * 1024;
+
+template <int BN>
+constexpr int stages_for() {
+  return (int)((kSmemBudget - 2048) / (size_t)(BM * BK * 2 + BN * BK * 2)) > 8
+             ? 8
+             : (int)((kSmemBudget - 2048) / (size_t)(BM * BK * 2 + BN * BK * 2));
+}
+
+template <int BN>
+cudaError_t run(const dpp_conv_desc &d, const CUtensorMap &mx, const CUtensorMap &ms,
+                const void *w, const float *bias, void *y, int use_stale, int *status,
+                cudaStream_t s) {
+  constexpr int STAGES = stages_for<BN>();
+  CUtensorMap mw;
+  {
+    const uint64_t dims[3] = {(uint64_t)d.C_in, 9, (uint64_t)d.C_out};
+    const uint64_t str[2] = {(uint64_t)d.C_in * 2, (uint64_t)d.C_in * 9 * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)BN};
+    if (!encode_tiled(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  ConvTcParams p;
+  p.B = d.B; p.H = d.H; p.W = d.W; p.Cin = d.C_in; p.Cout = d.C_out; p.P = d.P;
+  p.nseg = (d.W + BM - 1) / BM;
+  p.cblocks = (d.C_in + BK - 1) / BK;
+  p.m_tiles = d.B * d.H * p.nseg;
+  p.n_tiles = (d.C_out + BN - 1) / BN;
+  p.use_stale = use_stale;
+  p.bias = bias;
+  p.y = reinterpret_cast<__nv_bfloat16 *>(y);
+  p.status = status;
+  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512;
+  static_assert(smem <= kSmemBudget, "shared memory budget");
+  auto k = conv_tc_kernel<BN, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long tiles = (long long)p.m_tiles * p.n_tiles;
+  const int grid = tiles < sms ? (int)tiles : sms;
+  k<<<grid, kThreads, smem, s>>>(mx, ms, mw, p);
+  return cudaGetLastError();
+}
+
+// N tile for C_out: the candidate with the least padded work (tiles x BN),
+// the larger one on ties.
+int pick_bn(int cout) {
+  const int cands[4] = {64, 128, 160, 256};
+  int best = 0;
+  long long best_work = -1;
+  for (int bn : cands) {
+    const long long work = (long long)((cout + bn - 1) / bn) * bn;
+    if (best_work < 0 || work <= best_work) {
+      best = bn;
+      best_work = work;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+bool conv_tc_supported(const dpp_conv_desc &d) {
+  return d.dtype == DPP_BF16 && d.C_in % 8 == 0 && d.C_out % 8 == 0 && d.H % d.P == 0 &&
+         (long long)d.B * d.H * ((d.W + BM - 1) / BM) < (1ll << 31);
+}
+
+cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *stale,
+                           const void *w, const float *bias, void *y, int *status,
+                           cudaStream_t s) {
+  if (!conv_tc_supported(d)) return cudaErrorNotSupported;
+  const int use_stale = (stale && stale != x && !d.first_layer) ? 1 : 0;
+  CUtensorMap mx, ms;
+  const uint64_t dims[4] = {(uint64_t)d.C_in, (uint64_t)d.W, (uint64_t)d.H, (uint64_t)d.B};
+  const uint64_t str[3] = {(uint64_t)d.C_in * 2, (uint64_t)d.W * d.C_in * 2,
+                           (uint64_t)d.H * d.W * d.C_in * 2};
+  const uint32_t box[4] = {64, 128, 1, 1};
+  if (!encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tiled(&ms, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, use_stale ? stale : x, dims, str,
+                    box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  switch (pick_bn(d.C_out)) {
+    case 64: return run<64>(d, mx, ms, w, bias, y, use_stale, status, s);
+    case 128: return run<128>(d, mx, ms, w, bias, y, use_stale, status, s);
+    case 160: return run<160>(d, mx, ms, w, bias, y, use_stale, status, s);
+    default: return run<256>(d, mx, ms, w, bias, y, use_stale, status, s);
+  }
+}
+
+}  // namespace dpp
