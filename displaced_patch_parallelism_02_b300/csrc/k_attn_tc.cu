@@ -18,12 +18,23 @@
 //                   S_t = Q_t K^T   (M 128, N 128, K 64) into TMEM,
 //                   O_t += P_t V    (M 128, N 64, K 128) with P_t in shared
 //                                   memory (K-major) and V used MN-major.
-//   warps 4..7    softmax of query tile 0, warps 8..11 of tile 1: one thread
-//                 per query row (= TMEM lane); masked row max, p = 2^(s - m),
-//                 P written as fp16 in the 128-byte-swizzled layout, running
-//                 sum; the reference max m only moves when a row max exceeds
-//                 it by 8 (in log2 units), so the O accumulator in TMEM is
+//   warps 2..5    softmax of query tile 0, warps 6..9 of tile 1: one thread
+//                 per query row (= TMEM lane); row max (3-input max, four
+//                 independent chains), p = 2^(s*scale - m) with the scale
+//                 folded into paired fp32 FMAs, P written as fp16 in the
+//                 128-byte-swizzled layout, running sum in paired fp32 adds;
+//                 the reference max m only moves when a row max exceeds it
+//                 by 8 (in log2 units), so the O accumulator in TMEM is
 //                 rarely rescaled; final O / l stored as fp16.
+//
+// The exponentials are the softmax's bottleneck at head_dim 64 (one 2^x per
+// 128 tensor-core FLOPs, and the special-function unit retires a quarter of
+// the FP32 pipe's rate), so DPP_ATTN_POLY_EXP2 of every 8 are computed on
+// the FMA pipe instead: Cody-Waite range reduction x = n + f, n = rint(x)
+// (the 1.5 * 2^23 rounding trick), 2^f from a degree-3 polynomial whose
+// coefficients are a minimax (Remez exchange) fit of relative error on
+// [-1/2, 1/2] (max relative error 7.5e-5, below the 2^-11 rounding of the
+// fp16 P it feeds), and 2^n added to the exponent field.
 #include "tc_common.cuh"
 
 namespace dpp {
@@ -31,7 +42,14 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 384;
+#ifndef DPP_ATTN_POLY_EXP2
+#define DPP_ATTN_POLY_EXP2 3
+#endif
+constexpr int kPolyPer8 = DPP_ATTN_POLY_EXP2;
+static_assert(kPolyPer8 >= 0 && kPolyPer8 <= 8 && kPolyPer8 % 2 == 0 || kPolyPer8 == 3,
+              "pairs of polynomial exponentials, or 3 (one pair and one single)");
+
+constexpr int kThreads = 320;
 constexpr int KS = 3, VS = 3;  // K and V ring depths
 constexpr uint32_t TILE_BYTES = 128 * 128;  // 128 rows x 64 fp16
 constexpr uint32_t OFF_Q = 0;
@@ -81,22 +99,78 @@ __device__ __forceinline__ Segs make_segs(const AttnTcParams &p, int band) {
 }
 
 __device__ __forceinline__ KvTile tile_of(const Segs &s, int j) {
-  int i = 0;
-  while (j >= s.ntiles[i]) {
-    j -= s.ntiles[i];
-    ++i;
-  }
-  const int lo = s.lo[i], hi = s.hi[i], L = hi - lo;
+  // segment i holding tile j, selected without indexing the arrays by a
+  // runtime value (which would put them in local memory)
+  const bool in0 = j < s.ntiles[0];
+  const bool in1 = !in0 && j < s.ntiles[0] + s.ntiles[1];
+  const int lo = in0 ? s.lo[0] : (in1 ? s.lo[1] : s.lo[2]);
+  const int hi = in0 ? s.hi[0] : (in1 ? s.hi[1] : s.hi[2]);
+  const int nt = in0 ? s.ntiles[0] : (in1 ? s.ntiles[1] : s.ntiles[2]);
+  const int jj = in0 ? j : (in1 ? j - s.ntiles[0] : j - s.ntiles[0] - s.ntiles[1]);
+  const int L = hi - lo;
   KvTile t;
-  t.fresh = s.fresh[i];
+  t.fresh = in0 ? s.fresh[0] : (in1 ? s.fresh[1] : s.fresh[2]);
   if (L < 128) {
     t.kv0 = lo; t.vlo = 0; t.vhi = L;
-  } else if (j == s.ntiles[i] - 1 && (L & 127)) {
-    t.kv0 = hi - 128; t.vlo = lo + 128 * j - t.kv0; t.vhi = 128;
+  } else if (jj == nt - 1 && (L & 127)) {
+    t.kv0 = hi - 128; t.vlo = lo + 128 * jj - t.kv0; t.vhi = 128;
   } else {
-    t.kv0 = lo + 128 * j; t.vlo = 0; t.vhi = 128;
+    t.kv0 = lo + 128 * jj; t.vlo = 0; t.vhi = 128;
   }
   return t;
+}
+
+// ---- paired fp32 arithmetic (sm_100 family) and the exponential
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// 2^x for a pair of arguments on the FMA pipe (see the file comment).
+// Arguments below -126 (including the -inf of masked keys) are clamped, so
+// the result is at most 2^-126: zero once rounded to fp16.
+constexpr float kC0 = 0.99992805719375610f, kC1 = 0.69326096773147583f,
+                kC2 = 0.24261112511157990f, kC3 = 0.05517166852951050f;
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
+  float a, b;
+  f2unpack(x2, a, b);
+  x2 = f2pack(fmaxf(a, -126.f), fmaxf(b, -126.f));
+  const uint64_t t = fadd2(x2, f2pack(12582912.f, 12582912.f));   // n in the low mantissa bits
+  const uint64_t n = fadd2(t, f2pack(-12582912.f, -12582912.f));  // rint(x)
+  const uint64_t f = ffma2(n, f2pack(-1.f, -1.f), x2);            // x - n, in [-1/2, 1/2]
+  uint64_t p = ffma2(f2pack(kC3, kC3), f, f2pack(kC2, kC2));
+  p = ffma2(p, f, f2pack(kC1, kC1));
+  p = ffma2(p, f, f2pack(kC0, kC0));
+  float pa, pb, ta, tb;
+  f2unpack(p, pa, pb);
+  f2unpack(t, ta, tb);
+  return f2pack(__int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23)),
+                __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23)));
+}
+
+__device__ __forceinline__ uint64_t exp2_mufu2(uint64_t x2) {
+  float a, b;
+  f2unpack(x2, a, b);
+  return f2pack(ex2_approx(a), ex2_approx(b));
 }
 
 // Warp-uniform bounded wait: every lane waits, then the warp agrees.
@@ -247,8 +321,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         mbar_drain(drain, 0);
       }
     }
-  } else if (warp >= 4) {  // --------------------------------------- softmax
-    const int t = (warp - 4) / 4;
+  } else {  // ------------------------------------------------------ softmax
+    const int t = (warp - 2) / 4;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -270,14 +344,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&s_empty[t]);
-      float mx = -INFINITY;
+      if (kt.vlo != 0 || kt.vhi != 128) {  // ragged tile (uniform branch): mask
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const float v = (i >= kt.vlo && i < kt.vhi) ? __uint_as_float(sr[i]) * p.scale_log2
-                                                     : -INFINITY;
-        sr[i] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int i = 0; i < 128; ++i)
+          if (i < kt.vlo || i >= kt.vhi) sr[i] = 0xff800000u;  // -inf
       }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 128; i += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          m4[k] = max3f(m4[k], __uint_as_float(sr[i + 2 * k]), __uint_as_float(sr[i + 2 * k + 1]));
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
       float corr = 1.f;
       if (mx > m_ref + kRescaleThreshold) {
         corr = ex2_approx(m_ref - mx);  // 0 on the first tile
@@ -286,8 +364,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       l *= corr;
       if (!warp_wait(&p_empty[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // rescale O (rare)
+      const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_ref, -m_ref);
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
+      for (int c = 0; c < 16; ++c) {  // 16-byte chunk c holds keys 8c .. 8c+7
+        uint4 v;
+        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint64_t x2 = ffma2(f2pack(__uint_as_float(sr[8 * c + 2 * e]),
+                                           __uint_as_float(sr[8 * c + 2 * e + 1])),
+                                    sc2, nm2);
+          uint64_t e2;
+          if (2 * e + 1 < kPolyPer8) {
+            e2 = exp2_poly2(x2);
+          } else if (2 * e < kPolyPer8) {  // one of the pair on each unit
+            float xa, xb;
+            f2unpack(x2, xa, xb);
+            float pa, pb;
+            f2unpack(exp2_poly2(f2pack(xa, xa)), pa, pb);
+            e2 = f2pack(pa, ex2_approx(xb));
+          } else {
+            e2 = exp2_mufu2(x2);
+          }
+          acc2[e] = fadd2(acc2[e], e2);
+          float a, bb;
+          f2unpack(e2, a, bb);
+          w[e] = pack_half2(a, bb);
+        }
+        *reinterpret_cast<uint4 *>(Pt + (c >> 3) * TILE_BYTES + row * 128 +
+                                   ((((uint32_t)c & 7u) ^ swz) << 4)) = v;
+      }
+      // O of the keys so far is rescaled after P (and the scores) are out of
+      // registers; PV(j-1) has completed (p_empty) and PV(j) waits for p_full
+      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // rare
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
           tmem_ld32(tO + 32 * c, r);
@@ -298,22 +409,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
         tmem_wait_st();
       }
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {  // 16-byte chunk c holds keys 8c .. 8c+7
-        uint4 v;
-        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = ex2_approx(__uint_as_float(sr[8 * c + 2 * e]) - m_ref);
-          const float bb = ex2_approx(__uint_as_float(sr[8 * c + 2 * e + 1]) - m_ref);
-          sum += a + bb;
-          w[e] = pack_half2(a, bb);
-        }
-        *reinterpret_cast<uint4 *>(Pt + (c >> 3) * TILE_BYTES + row * 128 +
-                                   ((((uint32_t)c & 7u) ^ swz) << 4)) = v;
+      {
+        float a, bb;
+        f2unpack(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), a, bb);
+        l += a + bb;
       }
-      l += sum;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[t]);
