@@ -7,34 +7,35 @@
 // fp32 accumulators and softmax.  One CTA handles two 128-query tiles of one
 // band so that one tile's softmax overlaps the other tile's MMAs:
 //   warp 0        TMA producer: both Q tiles once, then K and V tiles of 128
-//                 keys into 3-deep rings (128-byte swizzle).  The key range is
+//                 keys into 4-deep rings (128-byte swizzle).  The key range is
 //                 walked segment by segment -- own band from the fresh state,
 //                 the keys before and after it from the stale state -- so each
 //                 tile has one source; a segment's ragged last tile is aligned
 //                 to end at the segment end (masking its leading columns), so
 //                 no tile reads outside its segment when the segment holds at
 //                 least 128 keys.
-//   warp 1        TMEM owner and single-thread MMA issuer:
-//                   S_t = Q_t K^T   (M 128, N 128, K 64) into TMEM,
-//                   O_t += P_t V    (M 128, N 64, K 128) with P_t in shared
-//                                   memory (K-major) and V used MN-major.
+//   warps 1, 10   one MMA-issuing thread per query tile t (warp 1 also owns
+//                 the TMEM allocation):
+//                   S_t = Q_t K^T   (M 128, N 128, K 64), both from shared memory,
+//                   O_t += P_t V    (M 128, N 64, K 128), P_t read from tensor
+//                                   memory, V from shared memory (MN-major);
+//                 separate issuers keep one tile's wait for its softmax from
+//                 stalling the other tile's MMAs.
 //   warps 2..5    softmax of query tile 0, warps 6..9 of tile 1: one thread
 //                 per query row (= TMEM lane); row max (3-input max, four
 //                 independent chains), p = 2^(s*scale - m) with the scale
-//                 folded into paired fp32 FMAs, P written as fp16 in the
-//                 128-byte-swizzled layout, running sum in paired fp32 adds;
-//                 the reference max m only moves when a row max exceeds it
-//                 by 8 (in log2 units), so the O accumulator in TMEM is
-//                 rarely rescaled; final O / l stored as fp16.
+//                 folded into paired fp32 FMAs and the exponentials on the
+//                 special-function unit, running sum in paired fp32 adds, P
+//                 written back to tensor memory as fp16 pairs; the reference
+//                 max m only moves when a row max exceeds it by 8 (in log2
+//                 units), so the O accumulator in TMEM is rarely rescaled;
+//                 final O / l stored as fp16.
 //
-// The exponentials are the softmax's bottleneck at head_dim 64 (one 2^x per
-// 128 tensor-core FLOPs, and the special-function unit retires a quarter of
-// the FP32 pipe's rate), so DPP_ATTN_POLY_EXP2 of every 8 are computed on
-// the FMA pipe instead: Cody-Waite range reduction x = n + f, n = rint(x)
-// (the 1.5 * 2^23 rounding trick), 2^f from a degree-3 polynomial whose
-// coefficients are a minimax (Remez exchange) fit of relative error on
-// [-1/2, 1/2] (max relative error 7.5e-5, below the 2^-11 rounding of the
-// fp16 P it feeds), and 2^n added to the exponent field.
+// Tensor memory per query tile t (256 columns at t * 256): S in columns
+// [0, 128), O in [128, 192), P in [192, 256) (fp16 pairs).  Keeping P out of
+// shared memory leaves the shared-memory bandwidth to the MMA operand reads
+// (Q, K, V), and lets a tile's exponentials run while the previous PV MMA
+// still reads the previous P.
 #include "tc_common.cuh"
 
 namespace dpp {
@@ -42,21 +43,13 @@ namespace {
 
 using namespace tc;
 
-#ifndef DPP_ATTN_POLY_EXP2
-#define DPP_ATTN_POLY_EXP2 3
-#endif
-constexpr int kPolyPer8 = DPP_ATTN_POLY_EXP2;
-static_assert(kPolyPer8 >= 0 && kPolyPer8 <= 8 && kPolyPer8 % 2 == 0 || kPolyPer8 == 3,
-              "pairs of polynomial exponentials, or 3 (one pair and one single)");
-
-constexpr int kThreads = 320;
-constexpr int KS = 3, VS = 3;  // K and V ring depths
+constexpr int kThreads = 352;  // 11 warps
+constexpr int KS = 4, VS = 4;  // K and V ring depths
 constexpr uint32_t TILE_BYTES = 128 * 128;  // 128 rows x 64 fp16
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
-constexpr uint32_t OFF_P = OFF_V + VS * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + 2 * 2 * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
 constexpr float kRescaleThreshold = 8.f;
 
@@ -145,28 +138,6 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   return r;
 }
 
-// 2^x for a pair of arguments on the FMA pipe (see the file comment).
-// Arguments below -126 (including the -inf of masked keys) are clamped, so
-// the result is at most 2^-126: zero once rounded to fp16.
-constexpr float kC0 = 0.99992805719375610f, kC1 = 0.69326096773147583f,
-                kC2 = 0.24261112511157990f, kC3 = 0.05517166852951050f;
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
-  float a, b;
-  f2unpack(x2, a, b);
-  x2 = f2pack(fmaxf(a, -126.f), fmaxf(b, -126.f));
-  const uint64_t t = fadd2(x2, f2pack(12582912.f, 12582912.f));   // n in the low mantissa bits
-  const uint64_t n = fadd2(t, f2pack(-12582912.f, -12582912.f));  // rint(x)
-  const uint64_t f = ffma2(n, f2pack(-1.f, -1.f), x2);            // x - n, in [-1/2, 1/2]
-  uint64_t p = ffma2(f2pack(kC3, kC3), f, f2pack(kC2, kC2));
-  p = ffma2(p, f, f2pack(kC1, kC1));
-  p = ffma2(p, f, f2pack(kC0, kC0));
-  float pa, pb, ta, tb;
-  f2unpack(p, pa, pb);
-  f2unpack(t, ta, tb);
-  return f2pack(__int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23)),
-                __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23)));
-}
-
 __device__ __forceinline__ uint64_t exp2_mufu2(uint64_t x2) {
   float a, b;
   f2unpack(x2, a, b);
@@ -193,7 +164,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   uint64_t *s_full = v_empty + VS, *s_empty = s_full + 2;
   uint64_t *p_full = s_empty + 2, *p_empty = p_full + 2;
   uint64_t *o_final = p_empty + 2, *drain = o_final + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -207,16 +178,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
-    for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
+    // a K or V slot is free once both query tiles' MMAs have read it
+    for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 2); }
+    for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 2); }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&s_empty[t], 128);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&s_empty[t], 4);  // one arrival per softmax warp
+      mbar_init(&p_full[t], 4);
       mbar_init(&p_empty[t], 1);
       mbar_init(&o_final[t], 1);
+      mbar_init(&drain[t], 1);
     }
-    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -265,60 +237,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           if ((v_armed >> i) & 1u) mbar_drain(&v_full[i], (v_par >> i) & 1u);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 10) {
+    if (lane == 0) {  // ------------------------- MMA issuer of query tile t
+      // Each query tile has its own issuing thread, so one tile's wait for
+      // its softmax never holds back the other tile's MMAs.  Per key tile j:
+      // S(j) = Q K(j)^T as soon as the softmax has read S(j-1), then
+      // O += P(j-1) V(j-1) once it has written P(j-1).
+      const int t = warp == 1 ? 0 : 1;
       constexpr uint32_t IDESC_S = idesc_f16(128, 128, false);
       constexpr uint32_t IDESC_O = idesc_f16(128, 64, false, true);
-      const uint32_t sQ = smem_u32(smem + OFF_Q), sK = smem_u32(smem + OFF_K);
-      const uint32_t sV = smem_u32(smem + OFF_V), sP = smem_u32(smem + OFF_P);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      auto qk = [&](int j, int t) -> bool {
-        if (!mbar_wait(&s_empty[t], (j & 1) ^ 1u, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint64_t ad = desc_sw128_kmajor(sQ + t * TILE_BYTES);
-        const uint64_t bd = desc_sw128_kmajor(sK + (j % KS) * TILE_BYTES);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mma_f16_ss(tmem + t * 256, ad + 2 * k, bd + 2 * k, IDESC_S, k);
-        mma_commit(&s_full[t]);
-        return true;
-      };
-      auto pv = [&](int j, int t) -> bool {
+      const uint32_t sQ = smem_u32(smem + OFF_Q) + t * TILE_BYTES, sK = smem_u32(smem + OFF_K);
+      const uint32_t sV = smem_u32(smem + OFF_V);
+      const uint32_t dS = tmem + t * 256, dO = dS + 128, aP = dS + 192;
+      auto pv = [&](int j) -> bool {  // O += P(j) V(j)
+        if (!mbar_wait(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&p_full[t], j & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t pb = sP + t * 2 * TILE_BYTES;
         const uint32_t vb = sV + (j % VS) * TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = desc_sw128_kmajor(pb + (kk >> 2) * TILE_BYTES) + 2 * (kk & 3);
-          const uint64_t bd = desc_sw128_mnmajor(vb + kk * 2048, 1024);
-          mma_f16_ss(tmem + t * 256 + 128, ad, bd, IDESC_O, (j | kk) != 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of P, 16 rows of V
+          mma_f16_ts(dO, aP + kk * 8, desc_sw128_mnmajor(vb + kk * 2048, 1024), IDESC_O,
+                     (j | kk) != 0);
         mma_commit(&p_empty[t]);
+        mma_commit(&v_empty[j % VS]);
         return true;
       };
-      if (ok && T > 0) {
-        ok = mbar_wait(&k_full[0], 0, abort_flag, p.status) && qk(0, 0) && qk(0, 1);
-        if (ok) mma_commit(&k_empty[0]);
-      }
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      const uint64_t ad = desc_sw128_kmajor(sQ);
       for (int j = 0; ok && j < T; ++j) {
-        const bool next = j + 1 < T;
-        if (next) ok = mbar_wait(&k_full[(j + 1) % KS], ((j + 1) / KS) & 1, abort_flag, p.status);
-        ok = ok && mbar_wait(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status);
-        if (ok && next) ok = qk(j + 1, 0);
-        ok = ok && pv(j, 0);
-        if (ok && next) {
-          ok = qk(j + 1, 1);
-          if (ok) mma_commit(&k_empty[(j + 1) % KS]);
-        }
-        ok = ok && pv(j, 1);
-        if (ok) mma_commit(&v_empty[j % VS]);
+        ok = mbar_wait(&k_full[j % KS], (j / KS) & 1, abort_flag, p.status) &&
+             mbar_wait(&s_empty[t], (j & 1) ^ 1u, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t bd = desc_sw128_kmajor(sK + (j % KS) * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_f16_ss(dS, ad + 2 * k, bd + 2 * k, IDESC_S, k);
+        mma_commit(&s_full[t]);
+        mma_commit(&k_empty[j % KS]);
+        if (j > 0) ok = pv(j - 1);
       }
+      if (ok && T > 0) ok = pv(T - 1);
       if (ok) {
-        mma_commit(&o_final[0]);
-        mma_commit(&o_final[1]);
+        mma_commit(&o_final[t]);
       } else {  // nothing may still be writing TMEM when it is freed
-        mma_commit(drain);
-        mbar_drain(drain, 0);
+        mma_commit(&drain[t]);
+        mbar_drain(&drain[t], 0);
       }
     }
   } else {  // ------------------------------------------------------ softmax
@@ -326,9 +289,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_base + t * 256, tO = tS + 128;
-    uint8_t *Pt = smem + OFF_P + t * 2 * TILE_BYTES;
-    const uint32_t swz = (uint32_t)(row & 7);
+    const uint32_t tS = tmem + lane_base + t * 256, tO = tS + 128, tP = tS + 192;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
@@ -343,7 +304,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&s_empty[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[t]);
       if (kt.vlo != 0 || kt.vhi != 128) {  // ragged tile (uniform branch): mask
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -362,42 +324,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         m_ref = mx;
       }
       l *= corr;
-      if (!warp_wait(&p_empty[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      tc_fence_after();
+      // p = 2^(s * scale - m_ref), packed as fp16 pairs into pk[0..63]
       const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_ref, -m_ref);
       uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {  // 16-byte chunk c holds keys 8c .. 8c+7
-        uint4 v;
-        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint64_t x2 = ffma2(f2pack(__uint_as_float(sr[8 * c + 2 * e]),
-                                           __uint_as_float(sr[8 * c + 2 * e + 1])),
-                                    sc2, nm2);
-          uint64_t e2;
-          if (2 * e + 1 < kPolyPer8) {
-            e2 = exp2_poly2(x2);
-          } else if (2 * e < kPolyPer8) {  // one of the pair on each unit
-            float xa, xb;
-            f2unpack(x2, xa, xb);
-            float pa, pb;
-            f2unpack(exp2_poly2(f2pack(xa, xa)), pa, pb);
-            e2 = f2pack(pa, ex2_approx(xb));
-          } else {
-            e2 = exp2_mufu2(x2);
-          }
-          acc2[e] = fadd2(acc2[e], e2);
-          float a, bb;
-          f2unpack(e2, a, bb);
-          w[e] = pack_half2(a, bb);
-        }
-        *reinterpret_cast<uint4 *>(Pt + (c >> 3) * TILE_BYTES + row * 128 +
-                                   ((((uint32_t)c & 7u) ^ swz) << 4)) = v;
+      for (int i = 0; i < 64; ++i) {
+        const uint64_t x2 =
+            ffma2(f2pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sc2, nm2);
+        const uint64_t e2 = exp2_mufu2(x2);
+        acc2[i & 3] = fadd2(acc2[i & 3], e2);
+        float a, bb;
+        f2unpack(e2, a, bb);
+        pk[i] = pack_half2(a, bb);
       }
-      // O of the keys so far is rescaled after P (and the scores) are out of
-      // registers; PV(j-1) has completed (p_empty) and PV(j) waits for p_full
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // rare
+      {
+        float a, bb;
+        f2unpack(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), a, bb);
+        l += a + bb;
+      }
+      // PV(j-1) must be done reading P and writing O before both are rewritten
+      if (!warp_wait(&p_empty[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      tmem_st32(tP, *reinterpret_cast<uint32_t (*)[32]>(&pk[0]));
+      tmem_st32(tP + 32, *reinterpret_cast<uint32_t (*)[32]>(&pk[32]));
+      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // rescale O (rare)
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
@@ -407,16 +358,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
           tmem_st32(tO + 32 * c, r);
         }
-        tmem_wait_st();
       }
-      {
-        float a, bb;
-        f2unpack(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), a, bb);
-        l += a + bb;
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
     if (ok && warp_wait(&o_final[t], 0, abort_flag, p.status)) {
       tc_fence_after();

@@ -8,10 +8,15 @@
 // the conditional minus the unconditional estimate).
 //
 // HBM-bound single pass: 16-byte loads of u and c, one 16-byte store.
-// Reduction: fp32 per thread over a handful of elements, fp64 from the warp
-// level up; block partials go to the workspace and the last block to finish
-// (a wrapping atomicInc counter, which it leaves at zero) adds them in block
-// order.  The grid depends only on n, so the sums are bit-reproducible.
+// Reduction: fp32 within a block (per thread, then a warp-shuffle tree, then
+// the 8 warp sums), fp64 across blocks; block partials go to the workspace
+// and the last block to finish (a wrapping atomicInc counter, which it
+// leaves at zero) adds them in a fixed order.  The grid depends only on n,
+// so the sums are bit-reproducible.  FP64 arithmetic runs at a small
+// fraction of the FP32 rate on this part, so it is kept to the few
+// additions per block that the cross-block combine needs; a block's fp32
+// tree over at most a few thousand terms carries a relative error of a few
+// times 2^-24.
 #include "dpp_internal.h"
 
 namespace dpp {
@@ -19,30 +24,16 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ double warp_sum(double v) {
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
 }
 
-// Sums three per-thread values over the block in a fixed order; result
-// valid in thread 0.
-__device__ __forceinline__ void block_sum3(double v[3], double (*sm)[3]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
-  for (int k = 0; k < 3; ++k) v[k] = warp_sum(v[k]);
-  if (lane == 0) {
-#pragma unroll
-    for (int k = 0; k < 3; ++k) sm[warp][k] = v[k];
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < 3; ++k) {
-      double t = 0.0;
-      for (int w = 0; w < kThreads / 32; ++w) t += sm[w][k];
-      v[k] = t;
-    }
-  }
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -73,12 +64,24 @@ cfg_kernel(const float *__restrict__ u, const float *__restrict__ c, float s, si
   }
   if (sums3 == nullptr) return;
 
-  __shared__ double sm[kThreads / 32][3];
+  __shared__ float sm[kThreads / 32][3];
   __shared__ bool is_last;
-  double v[3] = {a0, a1, a2};
-  block_sum3(v, sm);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a0 = warp_sum(a0);
+  a1 = warp_sum(a1);
+  a2 = warp_sum(a2);
+  if (lane == 0) {
+    sm[warp][0] = a0;
+    sm[warp][1] = a1;
+    sm[warp][2] = a2;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 3; ++k) partials[blockIdx.x * 3 + k] = v[k];
+    for (int k = 0; k < 3; ++k) {
+      double t = 0.0;
+      for (int w = 0; w < kThreads / 32; ++w) t += (double)sm[w][k];
+      partials[blockIdx.x * 3 + k] = t;
+    }
     __threadfence();
     const unsigned prev = atomicInc(counter, gridDim.x - 1);  // wraps to 0 on the last block
     is_last = (prev == gridDim.x - 1);
@@ -86,13 +89,12 @@ cfg_kernel(const float *__restrict__ u, const float *__restrict__ c, float s, si
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  double t[3] = {0.0, 0.0, 0.0};
-  for (unsigned b = threadIdx.x; b < gridDim.x; b += kThreads)
-    for (int k = 0; k < 3; ++k) t[k] += __ldcg(partials + b * 3 + k);
-  __syncthreads();  // sm reuse
-  block_sum3(t, sm);
-  if (threadIdx.x == 0)
-    for (int k = 0; k < 3; ++k) sums3[k] = t[k];
+  if (warp < 3) {  // warp k adds quantity k: lane l takes blocks l, l + 32, ...
+    double t = 0.0;
+    for (unsigned b = lane; b < gridDim.x; b += 32) t += __ldcg(partials + b * 3 + warp);
+    t = warp_sum(t);
+    if (lane == 0) sums3[warp] = t;
+  }
 }
 
 }  // namespace
