@@ -32,14 +32,10 @@ size_t cfg_blocks(size_t n);
 cudaError_t launch_cfg(const float *u, const float *c, float scale, size_t n, float *out,
                        double *sums3, void *ws, cudaStream_t s);
 
-// GroupNorm: partial-sum pass and normalise pass
-struct GnPlan {
-  int units;          // P * B
-  int chunks;         // chunks per unit
-  int pix_per_unit;   // (H / P) * W
-  int pix_per_chunk;
-};
-GnPlan gn_plan(const dpp_gn_desc &d);
+// GroupNorm: one cooperative launch (plus a counter reset), band-major, the
+// second read of each chunk served from L2.  The workspace holds per-unit
+// counters and fp64 totals; the grid is at most kGnMaxGrid CTAs.
+constexpr int kGnMaxGrid = 592;  // 148 SMs x 4 resident CTAs
 size_t gn_workspace(const dpp_gn_desc &d);
 cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *stats_prev,
                              float *stats_next, const float *gamma, const float *beta,

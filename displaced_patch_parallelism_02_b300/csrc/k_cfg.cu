@@ -90,8 +90,13 @@ cfg_kernel(const float *__restrict__ u, const float *__restrict__ c, float s, si
   if (!is_last) return;
   __threadfence();
   if (warp < 3) {  // warp k adds quantity k: lane l takes blocks l, l + 32, ...
-    double t = 0.0;
-    for (unsigned b = lane; b < gridDim.x; b += 32) t += __ldcg(partials + b * 3 + warp);
+    double t4[4] = {0.0, 0.0, 0.0, 0.0};  // independent sums: many L2 loads in flight
+    unsigned b = lane;
+    for (; b + 96 < gridDim.x; b += 128)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) t4[k] += __ldcg(partials + (b + 32 * k) * 3 + warp);
+    for (; b < gridDim.x; b += 32) t4[0] += __ldcg(partials + b * 3 + warp);
+    double t = (t4[0] + t4[1]) + (t4[2] + t4[3]);
     t = warp_sum(t);
     if (lane == 0) sums3[warp] = t;
   }
@@ -99,10 +104,14 @@ cfg_kernel(const float *__restrict__ u, const float *__restrict__ c, float s, si
 
 }  // namespace
 
+// Two blocks per SM: each thread keeps several 16-byte loads in flight and
+// the final combine adds few partials.  A function of n only.
+constexpr size_t kCfgMaxBlocks = 296;
+
 size_t cfg_blocks(size_t n) {
   size_t b = (n / 4 + kThreads - 1) / kThreads;
   if (b < 1) b = 1;
-  if (b > (size_t)kReduceBlocks) b = kReduceBlocks;
+  if (b > kCfgMaxBlocks) b = kCfgMaxBlocks;
   return b;
 }
 

@@ -139,7 +139,11 @@ dpp_status dpp_conv3x3(const dpp_conv_desc *desc, const void *x, const void *sta
  *                 for the synchronous step (statistics of x alone).
  *   stats_next  : [P, B, G, 2] fp32 output; must not overlap stats_prev.
  *   gamma, beta : [C] fp32, both NULL for no affine.
- *   ws          : dpp_groupnorm_workspace_bytes(desc) bytes of device memory.
+ *   ws          : dpp_groupnorm_workspace_bytes(desc) bytes of device memory,
+ *                 any contents (the call clears the counters it holds).
+ *                 Calls sharing a workspace must not overlap on the GPU.
+ * The kernel is a cooperative launch (all its CTAs resident at once), so
+ * it waits for the whole device when other work occupies it.
  * Requires H % P == 0, C % G == 0, C a multiple of 8 (bf16) / 4 (f32).
  * ------------------------------------------------------------------------- */
 dpp_status dpp_groupnorm(const dpp_gn_desc *desc, const void *x, const float *stats_prev,
@@ -158,15 +162,15 @@ size_t dpp_groupnorm_workspace_bytes(const dpp_gn_desc *desc);
  * static device array of DPP_GN_STATIC_SCRATCH_BYTES that every GPU loading
  * the library holds until the process exits.  It allocates nothing.
  *   - Returns DPP_ERR_WORKSPACE when dpp_groupnorm_workspace_bytes(desc)
- *     exceeds DPP_GN_STATIC_SCRATCH_BYTES (with G = 32 groups that needs
- *     about 4000 band x chunk units, far beyond any latent this library's
- *     partitioning produces).
+ *     exceeds DPP_GN_STATIC_SCRATCH_BYTES (512 bytes per batch x band
+ *     unit with G = 32 groups: about 2000 units).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
- *   - All calls share the array and it keeps the last call's contents:
- *     calls whose kernels overlap on the GPU (several streams or host
- *     threads) race on it.
+ *   - All calls share the array and it keeps the last call's contents
+ *     (each call clears the counters it needs before use): calls whose
+ *     kernels overlap on the GPU (several streams or host threads) race on
+ *     it.
  * ------------------------------------------------------------------------- */
 #define DPP_GN_STATIC_SCRATCH_BYTES (1u << 20)
 dpp_status dpp_groupnorm_static(const dpp_gn_desc *desc, const void *x,

@@ -188,8 +188,9 @@ def test_rejected_calls_launch_nothing():
 
 
 def test_static_groupnorm_rejects_oversize_scratch_on_the_host():
-    # 8192 groups of one channel over a 256x256 latent need ~38 MB of partials
-    big = gn(H=256, W=256, C=8192, G=8192, P=1)
+    # 8192 one-channel groups in 64 bands of 2 images: 128 units x 8192
+    # groups x 2 fp64 totals = 16 MiB of scratch
+    big = gn(B=2, H=256, W=256, C=8192, G=8192, P=64)
     assert dpp.dpp_groupnorm_workspace_bytes(big) > dpp.DPP_GN_STATIC_SCRATCH_BYTES
     before = dpp.dpp_launch_count()
     st = dpp.dpp_groupnorm_static(big, A, None, Ep, None, None, Dp, stream=0,
