@@ -72,6 +72,28 @@ def work_model(w):
     }
 
 
+def attn_traffic():
+    """DRAM bytes per launch of the attention core from the committed ncu
+    summary, or None when the kernel sources have changed since it was taken
+    (the summary records a SHA-256 of k_attn_tc.cu + tc_common.cuh)."""
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    try:
+        text = open(os.path.join(here, "profiles", "dram_bytes_sdxl_3840_cfg.md")).read()
+        rec = dict(l.strip().split(": ", 1) for l in text.splitlines()
+                   if l.strip().startswith("attn_tc_"))
+        h = hashlib.sha256()
+        for f in ("k_attn_tc.cu", "tc_common.cuh"):
+            with open(os.path.join(here, "displaced_patch_parallelism_02_b300", "csrc", f),
+                      "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest() != rec["attn_tc_source_sha256"]:
+            return None
+        return int(rec["attn_tc_dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -522,7 +544,9 @@ def main():
             "roofline": {"kernel": "self-attention core", "bound": "tensor",
                          "achieved": ops["self_attn_core"]["tflops"], "peak": sus,
                          "unit": "TFLOP/s", "frac": ops["self_attn_core"]["tflops"] / sus,
-                         "peak_source": f"{peak_src} bf16 sustained", "traffic": None},
+                         "peak_source": f"{peak_src} bf16 sustained",
+                         "traffic": attn_traffic() if w.name == "sdxl_3840_cfg" else None,
+                         "traffic_unit": "bytes per launch (ncu dram read + write)"},
             "ops": ops,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
