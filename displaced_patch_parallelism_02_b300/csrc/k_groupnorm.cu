@@ -19,16 +19,17 @@
 //         (one release increment, nothing waited for).  The partials are
 //         fp32 values of similar size, so their fp64 sum is exact and does
 //         not depend on arrival order;
-//   B(u)  once the counter shows the whole group (acquire loads; the group's
-//         first CTA then publishes the band's stats_next entry): rebuilds the
-//         band's statistics
+//   B(u)  after A of the group's next unit (so the group's barrier completes
+//         while that unit streams), once the counter shows the whole group
+//         (acquire loads; the group's first CTA then publishes the band's
+//         stats_next entry): rebuilds the band's statistics
 //         (fresh totals plus stale partials, fp64), folds mean/rstd/gamma/
 //         beta into one scale and shift per channel and normalises the chunk
-//         -- read again moments after A(u), so from L2 (evict-first hints on
-//         the re-read and on y).
-// x crosses HBM once and y once.  While one group waits at its barrier the
-// others stream, and the bulk copy of the group's next unit is already in
-// flight.  The synchronous step sums every unit first and then normalises
+//         -- read again one unit after A(u), mostly from L2 (evict-first hints
+//         on the re-read and on y).
+// y crosses HBM once and x a little more than once (the re-reads that miss
+// L2).  While one group waits at its barrier the others stream, and the bulk
+// copy of the group's next unit is already in flight.  The synchronous step sums every unit first and then normalises
 // (its statistics span all bands of an image), so there x is read twice.
 //
 // Every wait on a counter is bounded (DPP_ERR_TIMEOUT in the device
@@ -42,6 +43,7 @@ namespace dpp {
 namespace {
 
 constexpr uint64_t kGnWaitLimitNs = 1000000000ull;
+constexpr int kGnLag = 1;  // a group's units between a chunk's two reads
 
 __device__ __forceinline__ uint64_t gn_globaltimer() {
   uint64_t t;
@@ -413,9 +415,15 @@ gn_fused_kernel(const T *x, T *y, GnGeom g, const float *__restrict__ stats_prev
 
   bool ok = true;
   if (!g.sync) {
-    // each unit is normalised right after its group has summed it: the chunk
-    // was read moments ago and is still in L2
-    for (int u = grp; ok && u < g.units; u += g.groups) ok = pass_a(u) && pass_b(u);
+    // the group's k-th unit is normalised after its (k + kGnLag)-th is summed:
+    // the chunk was read moments ago and is still in L2, and the lag lets the
+    // group's barrier complete while the next unit streams
+    const int n = grp < g.units ? (g.units - grp + g.groups - 1) / g.groups : 0;
+    for (int k = 0; ok && k < n; ++k) {
+      ok = pass_a(grp + k * g.groups);
+      if (ok && k >= kGnLag) ok = pass_b(grp + (k - kGnLag) * g.groups);
+    }
+    for (int k = n - kGnLag < 0 ? 0 : n - kGnLag; ok && k < n; ++k) ok = pass_b(grp + k * g.groups);
   } else {
     // the synchronous step needs every band of an image first
     for (int u = grp; ok && u < g.units; u += g.groups) ok = pass_a(u);
@@ -442,7 +450,7 @@ size_t gn_pixel_bytes(const dpp_gn_desc &d) { return (size_t)d.C * (d.dtype == D
 
 // The prefetch buffer holds up to 64 KB of whole pixels.
 constexpr size_t kGnBufBytes = 64 * 1024;
-constexpr int kGnGroups = 8;
+constexpr int kGnGroups = 4;
 int gn_buf_pixels(const dpp_gn_desc &d) {
   const size_t n = kGnBufBytes / gn_pixel_bytes(d);
   return n < 1 ? 1 : (int)n;
@@ -472,6 +480,7 @@ cudaError_t run_gn(const dpp_gn_desc &d, const void *x, const float *stats_prev,
                    int *status, cudaStream_t s) {
   GnWs w;
   gn_layout(d, ws, &w);
+
   const int VPP = d.C / gn_vec(d), R = gn_rows(d);
   const int threads = R * VPP;
   const size_t smem = gn_smem(d);
