@@ -71,6 +71,10 @@ _SIGNATURES = {
     "dpp_groupnorm": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _sz, _vp]),
     "dpp_groupnorm_workspace_bytes": (_sz, [ctypes.POINTER(dpp_gn_desc)]),
+    "dpp_conv3x3_gn": (_st, [ctypes.POINTER(dpp_conv_desc), _vp, _vp, _vp, _vp, _vp,
+                             ctypes.c_int, _vp, _vp]),
+    "dpp_groupnorm_apply": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp]),
     "dpp_groupnorm_static": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp, _vp, _vp, _vp,
                                    _vp]),
     "dpp_self_attn": (_st, [ctypes.POINTER(dpp_attn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -149,6 +153,22 @@ def dpp_conv3x3(desc: dpp_conv_desc, x, stale_prev, w, bias, y, stream=None,
     return _check(lib.dpp_conv3x3(ctypes.byref(desc), _ptr(x), _ptr(stale_prev), _ptr(w),
                                   _ptr(bias), _ptr(y), _stream(stream)),
                   "dpp_conv3x3", raise_on_error)
+
+
+def dpp_conv3x3_gn(desc: dpp_conv_desc, x, stale_prev, w, bias, y, G: int, gn_sums,
+                   stream=None, raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_conv3x3_gn(ctypes.byref(desc), _ptr(x), _ptr(stale_prev), _ptr(w),
+                                     _ptr(bias), _ptr(y), int(G), _ptr(gn_sums),
+                                     _stream(stream)),
+                  "dpp_conv3x3_gn", raise_on_error)
+
+
+def dpp_groupnorm_apply(desc: dpp_gn_desc, x, stats_prev, gn_sums, stats_next, gamma, beta, y,
+                        stream=None, raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_groupnorm_apply(ctypes.byref(desc), _ptr(x), _ptr(stats_prev),
+                                          _ptr(gn_sums), _ptr(stats_next), _ptr(gamma),
+                                          _ptr(beta), _ptr(y), _stream(stream)),
+                  "dpp_groupnorm_apply", raise_on_error)
 
 
 def dpp_groupnorm_workspace_bytes(desc: dpp_gn_desc) -> int:

@@ -290,6 +290,51 @@ dpp_status dpp_conv3x3(const dpp_conv_desc *d, const void *x, const void *stale_
   return from_cuda(counted(launch_conv_simt(*d, x, stale_prev, w, bias, y, s), 1));
 }
 
+// ------------------------------------------- conv + GroupNorm, fused sums
+dpp_status dpp_conv3x3_gn(const dpp_conv_desc *d, const void *x, const void *stale_prev,
+                          const void *w, const float *bias, void *y, int G, double *gn_sums,
+                          dpp_stream stream) {
+  dpp_status st = check_conv(d, x, stale_prev, w, bias, y);
+  if (st != DPP_OK) return st;
+  if (!gn_sums || G < 1 || d->C_out % G) return DPP_ERR_INVALID_ARG;
+  if (!conv_tc_supported(*d)) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(gn_sums)) return DPP_ERR_ALIGN;
+  const size_t es = elem_size(d->dtype);
+  const long long pix = (long long)d->B * d->H * d->W;
+  const size_t ns = (size_t)d->P * d->B * G * 2 * sizeof(double);
+  if (overlap(gn_sums, ns, y, (size_t)pix * d->C_out * es) ||
+      overlap(gn_sums, ns, x, (size_t)pix * d->C_in * es) ||
+      overlap(gn_sums, ns, stale_prev, (size_t)pix * d->C_in * es) ||
+      overlap(gn_sums, ns, w, (size_t)d->C_out * 9 * d->C_in * es) ||
+      overlap(gn_sums, ns, bias, (size_t)d->C_out * sizeof(float)))
+    return DPP_ERR_ALIAS;
+  return from_cuda(counted(launch_conv_tc(*d, x, stale_prev, w, bias, y, device_status_ptr(),
+                                          (cudaStream_t)stream, gn_sums, G),
+                           2));
+}
+
+dpp_status dpp_groupnorm_apply(const dpp_gn_desc *d, const void *x, const float *stats_prev,
+                               const double *gn_sums, float *stats_next, const float *gamma,
+                               const float *beta, void *y, dpp_stream stream) {
+  dpp_status st = check_gn(d);
+  if (st != DPP_OK) return st;
+  if (!x || !y || !stats_next || !gn_sums) return DPP_ERR_INVALID_ARG;
+  if ((gamma == nullptr) != (beta == nullptr)) return DPP_ERR_INVALID_ARG;
+  if (d->G > 1024) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(stats_next) || !aligned16(gn_sums) ||
+      (stats_prev && !aligned16(stats_prev)))
+    return DPP_ERR_ALIGN;
+  const size_t nx = (size_t)d->B * d->H * d->W * d->C * elem_size(d->dtype);
+  const size_t ns = (size_t)d->P * d->B * d->G * 2 * sizeof(float);
+  if (y != x && overlap(y, nx, x, nx)) return DPP_ERR_ALIAS;
+  if (overlap(stats_prev, ns, stats_next, ns) || overlap(stats_next, ns, y, nx) ||
+      overlap(stats_next, ns, gn_sums, 2 * ns) || overlap(y, nx, gn_sums, 2 * ns))
+    return DPP_ERR_ALIAS;
+  return from_cuda(counted(launch_groupnorm_apply(*d, x, stats_prev, gn_sums, stats_next, gamma,
+                                                  beta, y, (cudaStream_t)stream),
+                           1));
+}
+
 // ---------------------------------------------------------------- attention
 size_t dpp_self_attn_workspace_bytes(const dpp_attn_desc *d) {
   if (check_attn(d, false) != DPP_OK) return 0;

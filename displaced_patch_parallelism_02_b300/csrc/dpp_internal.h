@@ -41,6 +41,12 @@ cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *s
                              float *stats_next, const float *gamma, const float *beta,
                              void *y, void *ws, cudaStream_t s);
 
+// GroupNorm's single pass given the band sums of its input (from the conv
+// epilogue): gn_sums fp64 [P][B][G][2].
+cudaError_t launch_groupnorm_apply(const dpp_gn_desc &d, const void *x, const float *stats_prev,
+                                   const double *gn_sums, float *stats_next, const float *gamma,
+                                   const float *beta, void *y, cudaStream_t s);
+
 // GroupNorm with its scratch in a static device array of this many bytes
 // (no workspace argument, no allocation).
 constexpr size_t kGnStaticScratchBytes = DPP_GN_STATIC_SCRATCH_BYTES;
@@ -55,9 +61,11 @@ cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *
 // tcgen05 implicit-GEMM conv (bf16); returns cudaErrorNotSupported when the
 // shape is outside what the kernel handles
 bool conv_tc_supported(const dpp_conv_desc &d);
+// With gn_sums (fp64 [P][B][G][2]) the epilogue also writes, per band,
+// image and group of G, the sum and sum of squares of the stored output.
 cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *stale,
                            const void *w, const float *bias, void *y, int *status,
-                           cudaStream_t s);
+                           cudaStream_t s, double *gn_sums = nullptr, int G = 0);
 
 // Element types inside the library.  Attention layers whose activations are
 // bf16 keep Q, O and the K/V state in fp16: the same tensor-core rate with

@@ -17,7 +17,10 @@
 //               [C_out][3][3][C_in], 128-byte swizzle, STAGES-deep ring;
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer
 //               (M 128, N BN, K 16), two accumulators 256 columns apart;
-//   warps 2..5  epilogue: tcgen05.ld, + bias, bf16, 16-byte stores.
+//   warps 2..5  epilogue: tcgen05.ld, + bias, bf16, 16-byte stores; with
+//               STATS also the per-group sums of the stored values (for a
+//               GroupNorm of this output), reduced over the warp's 32 pixels
+//               and added into fp64 totals per (band, image, group).
 #include "tc_common.cuh"
 
 namespace dpp {
@@ -34,12 +37,35 @@ struct ConvTcParams {
   const float *bias;
   __nv_bfloat16 *y;
   int *status;
+  double *gn_sums;  // [P][B][G][2] (sum y, sum y^2) per band, image and group; may be null
+  int G;            // groups (channels C_out / G each)
 };
 
 constexpr int kThreads = 192;
 constexpr int BM = 128, BK = 64;
 
-template <int BN, int STAGES>
+// Butterfly reduce-scatter over the warp: lane l ends with the sum over all
+// 32 lanes of a[l] (31 shuffles; a[] is clobbered).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&a)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) {
+    const bool up = (lane & k) != 0;
+#pragma unroll
+    for (int i = 0; i < k; ++i) {
+      const float send = up ? a[i] : a[i + k];
+      const float keep = up ? a[i + k] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+    }
+  }
+  return a[0];
+}
+
+// STATS: the epilogue also adds, per band, image and GroupNorm group, the
+// sum and the sum of squares of the values it stores (as rounded to bf16),
+// into p.gn_sums -- the fresh partials a displaced GroupNorm of this output
+// needs, so that GroupNorm is left with a single streaming pass.
+template <int BN, int STAGES, bool STATS>
 __global__ void __launch_bounds__(kThreads, 1)
 conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
                const __grid_constant__ CUtensorMap tmW, const ConvTcParams p) {
@@ -59,6 +85,8 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   uint64_t *drain = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // STATS: each epilogue warp's channel sums over its 32 pixels: [4][BN][2]
+  float *chs = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + 512);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -181,6 +209,7 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, r);
         tmem_wait_ld();
         const int n = n0 + c * 32;
+        float st1[32], st2[32];  // STATS: this pixel's stored values and their squares
         if (w < p.W && n < p.Cout) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -196,9 +225,55 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 ow[e] = pack_bf162(__uint_as_float(r[8 * v + 2 * e]) + bv[2 * e],
                                    __uint_as_float(r[8 * v + 2 * e + 1]) + bv[2 * e + 1]);
               *reinterpret_cast<uint4 *>(yrow + nv) = o;
+              if (STATS) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float lo = __uint_as_float(ow[e] << 16);
+                  const float hi = __uint_as_float(ow[e] & 0xffff0000u);
+                  st1[8 * v + 2 * e] = lo;
+                  st1[8 * v + 2 * e + 1] = hi;
+                }
+              }
+            } else if (STATS) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) st1[8 * v + e] = 0.f;
             }
           }
+        } else if (STATS) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) st1[e] = 0.f;
         }
+        if (STATS) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) st2[e] = st1[e] * st1[e];
+          const float t1 = warp_reduce_scatter32(st1);  // channel n + lane, this warp's pixels
+          const float t2 = warp_reduce_scatter32(st2);
+          float *dst = chs + ((q * BN) + c * 32 + lane) * 2;
+          dst[0] = t1;
+          dst[1] = t2;
+        }
+      }
+      if (STATS) {
+        // this warp's channel sums -> group sums -> fp64 totals.  fp32 sums of
+        // similar size add exactly in fp64, so the totals do not depend on
+        // the order the atomics land in.
+        __syncwarp();
+        const int cg = p.Cout / p.G;
+        const int n1 = min(n0 + BN, p.Cout);
+        const int g0 = n0 / cg, g1 = (n1 - 1) / cg;
+        const int h = rowid % p.H, b = rowid / p.H, band = h / Hp;
+        for (int g = g0 + lane; g <= g1; g += 32) {
+          const int c0 = max(g * cg, n0) - n0, c1 = min((g + 1) * cg, n1) - n0;
+          float s1 = 0.f, s2 = 0.f;
+          for (int ch = c0; ch < c1; ++ch) {
+            s1 += chs[(q * BN + ch) * 2];
+            s2 += chs[(q * BN + ch) * 2 + 1];
+          }
+          double *gs = p.gn_sums + (((size_t)band * p.B + b) * p.G + g) * 2;
+          atomicAdd(gs, (double)s1);
+          atomicAdd(gs + 1, (double)s2);
+        }
+        __syncwarp();  // the slice is rewritten by the next tile
       }
       tc_fence_before();
       __syncwarp();
@@ -216,18 +291,20 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 
 constexpr size_t kSmemBudget = 227 * 1024;
 
-template <int BN>
+template <int BN, bool STATS>
 constexpr int stages_for() {
-  return (int)((kSmemBudget - 2048) / (size_t)(BM * BK * 2 + BN * BK * 2)) > 8
+  return (int)((kSmemBudget - 2048 - (STATS ? 4 * BN * 2 * sizeof(float) : 0)) /
+               (size_t)(BM * BK * 2 + BN * BK * 2)) > 8
              ? 8
-             : (int)((kSmemBudget - 2048) / (size_t)(BM * BK * 2 + BN * BK * 2));
+             : (int)((kSmemBudget - 2048 - (STATS ? 4 * BN * 2 * sizeof(float) : 0)) /
+                     (size_t)(BM * BK * 2 + BN * BK * 2));
 }
 
-template <int BN>
+template <int BN, bool STATS>
 cudaError_t run(const dpp_conv_desc &d, const CUtensorMap &mx, const CUtensorMap &ms,
-                const void *w, const float *bias, void *y, int use_stale, int *status,
-                cudaStream_t s) {
-  constexpr int STAGES = stages_for<BN>();
+                const void *w, const float *bias, void *y, int use_stale, double *gn_sums,
+                int G, int *status, cudaStream_t s) {
+  constexpr int STAGES = stages_for<BN, STATS>();
   CUtensorMap mw;
   {
     const uint64_t dims[3] = {(uint64_t)d.C_in, 9, (uint64_t)d.C_out};
@@ -247,9 +324,12 @@ cudaError_t run(const dpp_conv_desc &d, const CUtensorMap &mx, const CUtensorMap
   p.bias = bias;
   p.y = reinterpret_cast<__nv_bfloat16 *>(y);
   p.status = status;
-  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512;
+  p.gn_sums = gn_sums;
+  p.G = G;
+  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512 +
+                          (STATS ? (size_t)4 * BN * 2 * sizeof(float) : 0);
   static_assert(smem <= kSmemBudget, "shared memory budget");
-  auto k = conv_tc_kernel<BN, STAGES>;
+  auto k = conv_tc_kernel<BN, STAGES, STATS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
@@ -279,6 +359,12 @@ int pick_bn(int cout) {
 
 }  // namespace
 
+__global__ void zero_f64_kernel(double *p, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    p[i] = 0.0;
+}
+
 bool conv_tc_supported(const dpp_conv_desc &d) {
   return d.dtype == DPP_BF16 && d.C_in % 8 == 0 && d.C_out % 8 == 0 && d.H % d.P == 0 &&
          (long long)d.B * d.H * ((d.W + BM - 1) / BM) < (1ll << 31);
@@ -286,7 +372,7 @@ bool conv_tc_supported(const dpp_conv_desc &d) {
 
 cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *stale,
                            const void *w, const float *bias, void *y, int *status,
-                           cudaStream_t s) {
+                           cudaStream_t s, double *gn_sums, int G) {
   if (!conv_tc_supported(d)) return cudaErrorNotSupported;
   const int use_stale = (stale && stale != x && !d.first_layer) ? 1 : 0;
   CUtensorMap mx, ms;
@@ -300,11 +386,27 @@ cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *st
   if (!encode_tiled(&ms, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, use_stale ? stale : x, dims, str,
                     box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  if (gn_sums) {  // the epilogue accumulates into it: start from zero
+    const size_t n = (size_t)d.P * d.B * G * 2;
+    zero_f64_kernel<<<(unsigned)((n + 255) / 256 < 148 ? (n + 255) / 256 : 148), 256, 0, s>>>(
+        gn_sums, n);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const bool st = gn_sums != nullptr;
   switch (pick_bn(d.C_out)) {
-    case 64: return run<64>(d, mx, ms, w, bias, y, use_stale, status, s);
-    case 128: return run<128>(d, mx, ms, w, bias, y, use_stale, status, s);
-    case 160: return run<160>(d, mx, ms, w, bias, y, use_stale, status, s);
-    default: return run<256>(d, mx, ms, w, bias, y, use_stale, status, s);
+    case 64:
+      return st ? run<64, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
+                : run<64, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
+    case 128:
+      return st ? run<128, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
+                : run<128, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
+    case 160:
+      return st ? run<160, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
+                : run<160, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
+    default:
+      return st ? run<256, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
+                : run<256, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
   }
 }
 

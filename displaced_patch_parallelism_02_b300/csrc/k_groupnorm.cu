@@ -543,6 +543,121 @@ cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *s
 }  // namespace dpp
 
 // ---------------------------------------------------------------------------
+// GroupNorm when the producing conv has already summed each band
+// (dpp_conv3x3_gn): one streaming pass.  A CTA takes one chunk of one
+// (batch, band) unit, rebuilds the band's statistics (its fresh sums plus
+// the other bands' stale partials, fp64), folds mean/rstd/gamma/beta into a
+// scale and shift per channel in shared memory and normalises its chunk with
+// 16-byte loads and stores, four in flight per thread (each thread always
+// holds the same channel vector, so its scale and shift stay in registers).
+// The first chunk of each unit publishes the band's fresh sums to
+// stats_next.
+namespace dpp {
+namespace {
+
+template <typename T>
+__global__ void __launch_bounds__(512)
+gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int ppc,
+                const double *__restrict__ gn_sums, const float *__restrict__ stats_prev,
+                float *__restrict__ stats_next, const float *__restrict__ gamma,
+                const float *__restrict__ beta, float eps) {
+  constexpr int VE = Vec16<T>::N;
+  __shared__ float mean_s[1024], rstd_s[1024];  // per group (G <= C/VE*VE <= 8192 checked on host)
+  const int unit = blockIdx.y, b = unit / P, p = unit % P;
+  const int cg = C / G, Hp = H / P;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    const double *fr = gn_sums + (((size_t)p * B + b) * G + g) * 2;
+    double t1 = fr[0], t2 = fr[1];
+    for (int q = 0; q < P; ++q) {
+      if (q == p) continue;
+      if (stats_prev) {
+        const float *sq = stats_prev + (((size_t)q * B + b) * G + g) * 2;
+        t1 += sq[0];
+        t2 += sq[1];
+      } else {
+        const double *fq = gn_sums + (((size_t)q * B + b) * G + g) * 2;
+        t1 += fq[0];
+        t2 += fq[1];
+      }
+    }
+    const double n = (double)H * W * cg;
+    const double mean = t1 / n;
+    const double var = fmax(t2 / n - mean * mean, 0.0);
+    mean_s[g] = (float)mean;
+    rstd_s[g] = (float)(1.0 / sqrt(var + (double)eps));
+    if (blockIdx.x == 0) {
+      float *sn = stats_next + (((size_t)p * B + b) * G + g) * 2;
+      sn[0] = (float)fr[0];
+      sn[1] = (float)fr[1];
+    }
+  }
+  __syncthreads();
+  // thread t always holds channel vector t % (C/VE): its scale and shift stay
+  // in registers; R pixel rows per pass, four passes' loads in flight
+  const int VPP = C / VE, R = blockDim.x / VPP;
+  const int v = threadIdx.x % VPP, r = threadIdx.x / VPP;
+  if (r >= R) return;
+  float sc[VE], sh[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    const int ch = v * VE + e, g = ch / cg;
+    const float a = rstd_s[g] * (gamma ? gamma[ch] : 1.f);
+    sc[e] = a;
+    sh[e] = (beta ? beta[ch] : 0.f) - mean_s[g] * a;
+  }
+  const int npix = Hp * W;
+  const int j0 = blockIdx.x * ppc, j1 = min(j0 + ppc, npix);
+  const size_t base = ((size_t)b * H + (size_t)p * Hp) * W;
+  const uint64_t drop = gn_policy_evict_first();
+  for (int j = j0 + r; j < j1; j += 4 * R) {
+    uint4 raw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      raw[k] = j + k * R < j1 ? gn_ld_hint(x + (base + j + k * R) * C + v * VE, drop)
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (j + k * R < j1) {
+        float f[VE];
+        Vec16<T>::cvt(raw[k], f);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) f[e] = fmaf(f[e], sc[e], sh[e]);
+        gn_st_hint(y + (base + j + k * R) * C + v * VE, Vec16<T>::pack(f), drop);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_groupnorm_apply(const dpp_gn_desc &d, const void *x, const float *stats_prev,
+                                   const double *gn_sums, float *stats_next, const float *gamma,
+                                   const float *beta, void *y, cudaStream_t s) {
+  if (d.G > 1024) return cudaErrorNotSupported;
+  const int VPP = d.C / gn_vec(d), R = gn_rows(d);
+  const int threads = R * VPP;
+  const int units = d.B * d.P;
+  const int npix = (d.H / d.P) * d.W;
+  int chunks = (4 * 148 + units - 1) / units;  // about four CTAs per SM in all
+  const int max_chunks = (npix + 4 * R - 1) / (4 * R);  // at least four passes per CTA
+  if (chunks > max_chunks) chunks = max_chunks;
+  if (chunks < 1) chunks = 1;
+  const int ppc = (npix + chunks - 1) / chunks;
+  dim3 grid((unsigned)chunks, (unsigned)units);
+  if (d.dtype == DPP_BF16)
+    gn_apply_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
+        (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc,
+        gn_sums, stats_prev, stats_next, gamma, beta, d.eps);
+  else
+    gn_apply_kernel<float><<<grid, threads, 0, s>>>(
+        (const float *)x, (float *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc, gn_sums, stats_prev,
+        stats_next, gamma, beta, d.eps);
+  return cudaGetLastError();
+}
+
+}  // namespace dpp
+
+// ---------------------------------------------------------------------------
 // Allocation-free GroupNorm.  Some callers cannot allocate device memory:
 // plugins that run inside a host program which owns the whole device-memory
 // budget (an inference server's pre-planned arena, a framework layer API

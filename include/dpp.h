@@ -179,6 +179,35 @@ dpp_status dpp_groupnorm_static(const dpp_gn_desc *desc, const void *x,
                                 dpp_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * dpp_conv3x3_gn + dpp_groupnorm_apply -- the conv followed by the displaced
+ * GroupNorm of its output (the ResNet block's conv -> GroupNorm of the U-Net
+ * the DistriFusion developer guide partitions, sections 卷积层拆分 and
+ * 归一化层拆分), with the GroupNorm's fresh partial sums produced by the
+ * conv's epilogue instead of a pass of their own.  Results equal
+ * dpp_conv3x3 followed by dpp_groupnorm on the same inputs (up to the
+ * order of floating-point additions).
+ *
+ * dpp_conv3x3_gn: dpp_conv3x3, and in the same call
+ *   gn_sums[p,b,g] = (sum y, sum y^2) over band p of image b and the
+ *                    C_out/G channels of group g, of y as stored.
+ *   gn_sums : [P, B, G, 2] fp64 device memory, overwritten.
+ *   Requires the bf16 tensor-core conv (DPP_ERR_UNSUPPORTED otherwise) and
+ *   C_out % G == 0.
+ *
+ * dpp_groupnorm_apply: dpp_groupnorm given gn_sums of x; one pass over x.
+ *   Band p's statistics are gn_sums[p] plus stats_prev[q] for q != p
+ *   (NULL stats_prev: all bands' gn_sums -- the synchronous step);
+ *   stats_next[p] = gn_sums[p] rounded to fp32 (the refresh of the state).
+ *   Other arguments and rules as dpp_groupnorm; no workspace; G <= 1024.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_conv3x3_gn(const dpp_conv_desc *desc, const void *x, const void *stale_prev,
+                          const void *w, const float *bias, void *y, int G, double *gn_sums,
+                          dpp_stream stream);
+dpp_status dpp_groupnorm_apply(const dpp_gn_desc *desc, const void *x, const float *stats_prev,
+                               const double *gn_sums, float *stats_next, const float *gamma,
+                               const float *beta, void *y, dpp_stream stream);
+
+/* ---------------------------------------------------------------------------
  * dpp_self_attn -- DistriSelfAttentionPP (section 注意力机制拆分 of the
  * DistriFusion developer guide, attn1).  For band p:
  *   Q = x[band p] wq^T;  K/V rows of band p's tokens are x[band p] wk^T /

@@ -74,6 +74,33 @@ def groupnorm(x, stats_prev, G, eps, gamma, beta, P, y=None, stream=None):
     return y, stats_next
 
 
+def conv_gn(x, stale, w, bias, P, G, stream=None):
+    """dpp_conv3x3_gn: returns (y, gn_sums [P,B,G,2] fp64) as device tensors."""
+    x = cuda(x)
+    stale = cuda(stale) if stale is not None and stale.device.type == "cpu" else stale
+    B, H, W, Ci = x.shape
+    Co = w.shape[0]
+    wd = cuda(w.permute(0, 2, 3, 1))  # [Co,3,3,Ci]
+    y = torch.empty((B, H, W, Co), dtype=x.dtype, device="cuda")
+    sums = torch.empty((P, B, G, 2), dtype=torch.float64, device="cuda")
+    d = dpp.dpp_conv_desc(B, H, W, Ci, Co, P, CODES[x.dtype], 0)
+    dpp.dpp_conv3x3_gn(d, x, stale, wd, cuda(bias), y, G, sums, stream=stream)
+    return y, sums
+
+
+def groupnorm_apply(x, stats_prev, gn_sums, G, eps, gamma, beta, P, y=None, stream=None):
+    """dpp_groupnorm_apply: returns (y, stats_next) as device tensors."""
+    x = cuda(x)
+    d = gn_desc(x, G, eps, P)
+    B = x.shape[0]
+    stats_next = torch.empty((P, B, G, 2), dtype=torch.float32, device="cuda")
+    if y is None:
+        y = torch.empty_like(x)
+    dpp.dpp_groupnorm_apply(d, x, cuda(stats_prev) if stats_prev is not None else None,
+                            gn_sums, stats_next, cuda(gamma), cuda(beta), y, stream=stream)
+    return y, stats_next
+
+
 # ------------------------------------------------------------ attention
 def attn_desc(x, H, W, heads, P, n_ctx=0, c_ctx=0):
     B, N, C = x.shape
