@@ -45,14 +45,28 @@ cfg_kernel(const float *__restrict__ u, const float *__restrict__ c, float s, si
   const float4 *u4 = reinterpret_cast<const float4 *>(u);
   const float4 *c4 = reinterpret_cast<const float4 *>(c);
   float4 *o4 = reinterpret_cast<float4 *>(out);
-  for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n4; i += stride) {
-    const float4 uu = __ldcs(u4 + i), cc = __ldcs(c4 + i);
-    const float dx = cc.x - uu.x, dy = cc.y - uu.y, dz = cc.z - uu.z, dw = cc.w - uu.w;
-    __stcs(o4 + i, make_float4(fmaf(s, dx, uu.x), fmaf(s, dy, uu.y), fmaf(s, dz, uu.z),
-                               fmaf(s, dw, uu.w)));
-    a0 += fabsf(dx) + fabsf(dy) + fabsf(dz) + fabsf(dw);
-    a1 += fabsf(uu.x) + fabsf(uu.y) + fabsf(uu.z) + fabsf(uu.w);
-    a2 += fabsf(cc.x) + fabsf(cc.y) + fabsf(cc.z) + fabsf(cc.w);
+  // four vectors of each map per thread per pass, all loads issued before
+  // any arithmetic: one DRAM round trip per pass instead of four
+  for (size_t i0 = (size_t)blockIdx.x * kThreads + threadIdx.x; i0 < n4; i0 += 4 * stride) {
+    float4 uu[4], cc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const size_t i = i0 + k * stride;
+      uu[k] = i < n4 ? __ldcs(u4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      cc[k] = i < n4 ? __ldcs(c4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const size_t i = i0 + k * stride;
+      const float4 a = uu[k], c = cc[k];
+      const float dx = c.x - a.x, dy = c.y - a.y, dz = c.z - a.z, dw = c.w - a.w;
+      if (i < n4)
+        __stcs(o4 + i, make_float4(fmaf(s, dx, a.x), fmaf(s, dy, a.y), fmaf(s, dz, a.z),
+                                   fmaf(s, dw, a.w)));
+      a0 += fabsf(dx) + fabsf(dy) + fabsf(dz) + fabsf(dw);
+      a1 += fabsf(a.x) + fabsf(a.y) + fabsf(a.z) + fabsf(a.w);
+      a2 += fabsf(c.x) + fabsf(c.y) + fabsf(c.z) + fabsf(c.w);
+    }
   }
   if (blockIdx.x == 0 && threadIdx.x < n - 4 * n4) {  // scalar tail (< 4 elements)
     const size_t i = 4 * n4 + threadIdx.x;

@@ -485,15 +485,39 @@ cudaError_t run_gn(const dpp_gn_desc &d, const void *x, const float *stats_prev,
   const int threads = R * VPP;
   const size_t smem = gn_smem(d);
   auto k = gn_fused_kernel<T>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   int dev = 0, sms = 0, per_sm = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem)) !=
-      cudaSuccess)
-    return e;
+  {
+    // the attribute and the occupancy query cost host time on every call:
+    // keep them per (device, block shape, shared memory)
+    struct Entry {
+      int dev, threads;
+      size_t smem;
+      int sms, per_sm;
+    };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int n_cache = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    int hit = -1;
+    for (int i = 0; i < n_cache; ++i)
+      if (cache[i].dev == dev && cache[i].threads == threads && cache[i].smem == smem) hit = i;
+    if (hit >= 0) {
+      sms = cache[hit].sms;
+      per_sm = cache[hit].per_sm;
+    } else {
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+          cudaSuccess)
+        return e;
+      if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem)) !=
+          cudaSuccess)
+        return e;
+      if (n_cache < 16) cache[n_cache++] = Entry{dev, threads, smem, sms, per_sm};
+    }
+  }
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   GnGeom g;
   g.B = d.B; g.H = d.H; g.W = d.W; g.C = d.C; g.G = d.G; g.P = d.P;
