@@ -35,6 +35,10 @@ DPP_ERR_ALIGN = 7
 DPP_F32 = 0
 DPP_BF16 = 1
 
+DPP_HALO_STALE = 0
+DPP_HALO_FRESH = 1
+DPP_HALO_ZERO = 2
+
 
 class DppError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -46,20 +50,20 @@ class DppError(RuntimeError):
 class dpp_conv_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
                 ("C_in", ctypes.c_int), ("C_out", ctypes.c_int), ("P", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("first_layer", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("halo", ctypes.c_int)]
 
 
 class dpp_gn_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
                 ("C", ctypes.c_int), ("G", ctypes.c_int), ("P", ctypes.c_int),
-                ("eps", ctypes.c_float), ("dtype", ctypes.c_int)]
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int), ("band_local", ctypes.c_int)]
 
 
 class dpp_attn_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
                 ("C", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("P", ctypes.c_int), ("n_ctx", ctypes.c_int), ("c_ctx", ctypes.c_int),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("band_local", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p

@@ -58,6 +58,7 @@ dpp_status check_conv(const dpp_conv_desc *d, const void *x, const void *stale, 
   if (d->B < 1 || d->H < 1 || d->W < 1 || d->C_in < 1 || d->C_out < 1 || d->P < 1)
     return DPP_ERR_INVALID_ARG;
   if (d->H % d->P != 0) return DPP_ERR_INVALID_ARG;
+  if (d->halo < DPP_HALO_STALE || d->halo > DPP_HALO_ZERO) return DPP_ERR_INVALID_ARG;
   const int q = chan_quantum(d->dtype);
   if (d->C_in % q || d->C_out % q) return DPP_ERR_INVALID_ARG;
   const long long pix = (long long)d->B * d->H * d->W;
@@ -384,7 +385,8 @@ dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, 
   cudaError_t e = gemm(qkv, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 2. displaced attention core
-  AttnArgs a{q, kv_next, kv_prev, o, d->B, d->H * d->W, d->H * d->W, C, d->heads, d->P, te};
+  AttnArgs a{q,      kv_next, d->band_local ? nullptr : kv_prev, o, d->B, d->H * d->W,
+             d->H * d->W, C,      d->heads, d->P, te, d->band_local ? 1 : 0};
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 3. output projection
@@ -424,7 +426,7 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
                kv, 2 * C, 2 * C, nullptr, 0, tl, tl, te};
   e = gemm(kvg, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
-  AttnArgs a{q, kv, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, te};
+  AttnArgs a{q, kv, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, te, 0};
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   const size_t nkvb = (size_t)d->B * d->n_ctx * 2 * d->C * elem_bytes(te);

@@ -110,6 +110,7 @@ struct AttnArgs {
   void *o;
   int B, Nq, Nkv, C, heads, P;
   Elem te;
+  int band_local;  // queries of a band attend over that band's (fresh) keys only
 };
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s);

@@ -56,6 +56,7 @@ constexpr float kRescaleThreshold = 8.f;
 struct AttnTcParams {
   int B, Nq, Nkv, C, P;
   int has_stale;
+  int band_local;  // keys of the query's own band only (naive patches)
   int tpb;  // CTAs per band (two query tiles each)
   void *o;
   int *status;
@@ -72,7 +73,12 @@ struct Segs {
 
 __device__ __forceinline__ Segs make_segs(const AttnTcParams &p, int band) {
   Segs s;
-  if (p.has_stale && p.Nkv == p.Nq) {
+  if (p.band_local && p.Nkv == p.Nq) {  // the band's own (fresh) keys only
+    const int Np = p.Nq / p.P;
+    s.lo[0] = band * Np; s.hi[0] = (band + 1) * Np; s.fresh[0] = 1;
+    s.lo[1] = s.hi[1] = s.lo[2] = s.hi[2] = 0;
+    s.fresh[1] = s.fresh[2] = 0;
+  } else if (p.has_stale && p.Nkv == p.Nq) {
     const int Np = p.Nq / p.P;
     s.lo[0] = band * Np;  s.hi[0] = (band + 1) * Np; s.fresh[0] = 1;
     s.lo[1] = 0;          s.hi[1] = band * Np;       s.fresh[1] = 0;
@@ -428,7 +434,7 @@ cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s) {
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int Np = a.Nq / a.P;
-  AttnTcParams p{a.B, a.Nq, a.Nkv, a.C, a.P, a.kv_stale != nullptr ? 1 : 0,
+  AttnTcParams p{a.B,       a.Nq, a.Nkv,  a.C, a.P, a.kv_stale != nullptr ? 1 : 0, a.band_local,
                  (Np + 255) / 256, a.o, status, 0.125f * 1.4426950408889634f};
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);

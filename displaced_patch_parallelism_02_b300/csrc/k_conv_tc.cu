@@ -34,6 +34,7 @@ struct ConvTcParams {
   int cblocks;   // 64-channel blocks of C_in
   int m_tiles, n_tiles;
   int use_stale; // 0: every input row comes from the fresh map
+  int zero_halo; // 1: rows outside the band read as zero (naive patches)
   const float *bias;
   __nv_bfloat16 *y;
   int *status;
@@ -132,15 +133,19 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int w0 = seg * BM;
         for (int kb = 0; kb < KB; ++kb) {
           const int tap = kb / p.cblocks, cb = kb - tap * p.cblocks;
-          const int hh = h + tap / 3 - 1, ww = w0 + tap % 3 - 1;
-          // rows outside [0, H) are zero-filled whichever map is used
-          const CUtensorMap *src = (p.use_stale && (hh < lo || hh >= hi)) ? &tmS : &tmX;
+          const int hh = h + tap / 3 - 1;
+          const bool halo_row = hh < lo || hh >= hi;
+          // rows outside [0, H) are zero-filled whichever map is used; a
+          // zero halo asks for row -1, which TMA fills with zeros as well
+          const int hc = (p.zero_halo && halo_row) ? -1 : hh;
+          const int ww = w0 + tap % 3 - 1;
+          const CUtensorMap *src = (p.use_stale && halo_row) ? &tmS : &tmX;
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
           uint8_t *sa = smem + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          tma_load_4d(sa, src, &full[stage], cb * BK, ww, hh, b);
+          tma_load_4d(sa, src, &full[stage], cb * BK, ww, hc, b);
           tma_load_3d(sa + A_BYTES, &tmW, &full[stage], cb * BK, tap, n0);
           if (++stage == STAGES) {
             stage = 0;
@@ -302,8 +307,8 @@ constexpr int stages_for() {
 
 template <int BN, bool STATS>
 cudaError_t run(const dpp_conv_desc &d, const CUtensorMap &mx, const CUtensorMap &ms,
-                const void *w, const float *bias, void *y, int use_stale, double *gn_sums,
-                int G, int *status, cudaStream_t s) {
+                const void *w, const float *bias, void *y, int use_stale, int zero_halo,
+                double *gn_sums, int G, int *status, cudaStream_t s) {
   constexpr int STAGES = stages_for<BN, STATS>();
   CUtensorMap mw;
   {
@@ -321,6 +326,7 @@ cudaError_t run(const dpp_conv_desc &d, const CUtensorMap &mx, const CUtensorMap
   p.m_tiles = d.B * d.H * p.nseg;
   p.n_tiles = (d.C_out + BN - 1) / BN;
   p.use_stale = use_stale;
+  p.zero_halo = zero_halo;
   p.bias = bias;
   p.y = reinterpret_cast<__nv_bfloat16 *>(y);
   p.status = status;
@@ -374,7 +380,8 @@ cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *st
                            const void *w, const float *bias, void *y, int *status,
                            cudaStream_t s, double *gn_sums, int G) {
   if (!conv_tc_supported(d)) return cudaErrorNotSupported;
-  const int use_stale = (stale && stale != x && !d.first_layer) ? 1 : 0;
+  const int use_stale = (stale && stale != x && d.halo == DPP_HALO_STALE) ? 1 : 0;
+  const int zero_halo = d.halo == DPP_HALO_ZERO ? 1 : 0;
   CUtensorMap mx, ms;
   const uint64_t dims[4] = {(uint64_t)d.C_in, (uint64_t)d.W, (uint64_t)d.H, (uint64_t)d.B};
   const uint64_t str[3] = {(uint64_t)d.C_in * 2, (uint64_t)d.W * d.C_in * 2,
@@ -396,17 +403,17 @@ cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *st
   const bool st = gn_sums != nullptr;
   switch (pick_bn(d.C_out)) {
     case 64:
-      return st ? run<64, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
-                : run<64, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
+      return st ? run<64, true>(d, mx, ms, w, bias, y, use_stale, zero_halo, gn_sums, G, status, s)
+                : run<64, false>(d, mx, ms, w, bias, y, use_stale, zero_halo, nullptr, 0, status, s);
     case 128:
-      return st ? run<128, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
-                : run<128, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
+      return st ? run<128, true>(d, mx, ms, w, bias, y, use_stale, zero_halo, gn_sums, G, status, s)
+                : run<128, false>(d, mx, ms, w, bias, y, use_stale, zero_halo, nullptr, 0, status, s);
     case 160:
-      return st ? run<160, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
-                : run<160, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
+      return st ? run<160, true>(d, mx, ms, w, bias, y, use_stale, zero_halo, gn_sums, G, status, s)
+                : run<160, false>(d, mx, ms, w, bias, y, use_stale, zero_halo, nullptr, 0, status, s);
     default:
-      return st ? run<256, true>(d, mx, ms, w, bias, y, use_stale, gn_sums, G, status, s)
-                : run<256, false>(d, mx, ms, w, bias, y, use_stale, nullptr, 0, status, s);
+      return st ? run<256, true>(d, mx, ms, w, bias, y, use_stale, zero_halo, gn_sums, G, status, s)
+                : run<256, false>(d, mx, ms, w, bias, y, use_stale, zero_halo, nullptr, 0, status, s);
   }
 }
 

@@ -182,6 +182,7 @@ struct GnGeom {
   int sms;    // SM count when the grid is whole waves of it, else 0
   int R;      // pixel rows in flight per CTA (threads = R * C / VE)
   int sync;   // 1: no stale statistics
+  int band_local;  // 1: each band's statistics over its own rows only
   int ppp;    // pixels per prefetched piece (the shared-memory buffer)
 };
 
@@ -349,7 +350,8 @@ gn_fused_kernel(const T *x, T *y, GnGeom g, const float *__restrict__ stats_prev
   // ---- B(u): band statistics, then normalise the chunk (second read: L2)
   auto pass_b = [&](int u) -> bool {
     const int b = u / g.P, p = u % g.P;
-    const int first = g.sync ? b * g.P : u, last = g.sync ? b * g.P + g.P - 1 : u;
+    const bool whole = g.sync && !g.band_local;  // statistics of every band of the image
+    const int first = whole ? b * g.P : u, last = whole ? b * g.P + g.P - 1 : u;
     if (!gn_wait_units(ws.arrive, first, last, (unsigned)gsize, &s_flag, status)) return false;
     if (rank == 0)  // the band's fresh partials: the refresh of the GroupNorm state
       for (int i = tid; i < 2 * g.G; i += nthr)
@@ -357,7 +359,11 @@ gn_fused_kernel(const T *x, T *y, GnGeom g, const float *__restrict__ stats_prev
             (float)__ldcg(ws.tot + (size_t)u * 2 * g.G + i);
     for (int gg = tid; gg < g.G; gg += nthr) {
       double t1 = 0.0, t2 = 0.0;
-      if (g.sync) {
+      if (g.band_local) {
+        const double *tu = ws.tot + ((size_t)u * g.G + gg) * 2;
+        t1 = __ldcg(tu);
+        t2 = __ldcg(tu + 1);
+      } else if (g.sync) {
         for (int q = 0; q < g.P; ++q) {
           const double *tq = ws.tot + ((size_t)(b * g.P + q) * g.G + gg) * 2;
           t1 += __ldcg(tq);
@@ -374,7 +380,7 @@ gn_fused_kernel(const T *x, T *y, GnGeom g, const float *__restrict__ stats_prev
           t2 += sq[1];
         }
       }
-      const double n = (double)g.H * g.W * cg;
+      const double n = (double)(g.band_local ? Hp : g.H) * g.W * cg;
       const double mean = t1 / n;
       const double var = fmax(t2 / n - mean * mean, 0.0);
       mean_s[gg] = (float)mean;
@@ -414,7 +420,7 @@ gn_fused_kernel(const T *x, T *y, GnGeom g, const float *__restrict__ stats_prev
   };
 
   bool ok = true;
-  if (!g.sync) {
+  if (!g.sync || g.band_local) {
     // the group's k-th unit is normalised after its (k + kGnLag)-th is summed:
     // the chunk was read moments ago and is still in L2, and the lag lets the
     // group's barrier complete while the next unit streams
@@ -499,7 +505,15 @@ cudaError_t run_gn(const dpp_gn_desc &d, const void *x, const float *stats_prev,
     static std::mutex mu;
     static Entry cache[16];
     static int n_cache = 0;
+    static size_t attr_max[64] = {};  // the kernel's dynamic shared-memory limit, per device
     std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (smem > attr_max[dev]) {  // the limit only ever grows, so it covers every shape seen
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+          cudaSuccess)
+        return e;
+      attr_max[dev] = smem;
+    }
     int hit = -1;
     for (int i = 0; i < n_cache; ++i)
       if (cache[i].dev == dev && cache[i].threads == threads && cache[i].smem == smem) hit = i;
@@ -507,9 +521,6 @@ cudaError_t run_gn(const dpp_gn_desc &d, const void *x, const float *stats_prev,
       sms = cache[hit].sms;
       per_sm = cache[hit].per_sm;
     } else {
-      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-          cudaSuccess)
-        return e;
       if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
       if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem)) !=
@@ -525,6 +536,7 @@ cudaError_t run_gn(const dpp_gn_desc &d, const void *x, const float *stats_prev,
   g.npix = (d.H / d.P) * d.W;
   g.R = R;
   g.sync = stats_prev == nullptr ? 1 : 0;
+  g.band_local = d.band_local ? 1 : 0;
   long long grid = (long long)per_sm * sms;
   if (grid > kGnMaxGrid) grid = kGnMaxGrid;
   // CTA groups work on different units at the same time, so one group's
@@ -581,7 +593,7 @@ namespace {
 
 template <typename T>
 __global__ void __launch_bounds__(512)
-gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int ppc,
+gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int ppc, int band_local,
                 const double *__restrict__ gn_sums, const float *__restrict__ stats_prev,
                 float *__restrict__ stats_next, const float *__restrict__ gamma,
                 const float *__restrict__ beta, float eps) {
@@ -592,7 +604,7 @@ gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int 
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
     const double *fr = gn_sums + (((size_t)p * B + b) * G + g) * 2;
     double t1 = fr[0], t2 = fr[1];
-    for (int q = 0; q < P; ++q) {
+    for (int q = 0; q < P && !band_local; ++q) {
       if (q == p) continue;
       if (stats_prev) {
         const float *sq = stats_prev + (((size_t)q * B + b) * G + g) * 2;
@@ -604,7 +616,7 @@ gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int 
         t2 += fq[1];
       }
     }
-    const double n = (double)H * W * cg;
+    const double n = (double)(band_local ? Hp : H) * W * cg;
     const double mean = t1 / n;
     const double var = fmax(t2 / n - mean * mean, 0.0);
     mean_s[g] = (float)mean;
@@ -671,10 +683,11 @@ cudaError_t launch_groupnorm_apply(const dpp_gn_desc &d, const void *x, const fl
   if (d.dtype == DPP_BF16)
     gn_apply_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
         (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc,
-        gn_sums, stats_prev, stats_next, gamma, beta, d.eps);
+        d.band_local ? 1 : 0, gn_sums, stats_prev, stats_next, gamma, beta, d.eps);
   else
     gn_apply_kernel<float><<<grid, threads, 0, s>>>(
-        (const float *)x, (float *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc, gn_sums, stats_prev,
+        (const float *)x, (float *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc, d.band_local ? 1 : 0,
+        gn_sums, stats_prev,
         stats_next, gamma, beta, d.eps);
   return cudaGetLastError();
 }

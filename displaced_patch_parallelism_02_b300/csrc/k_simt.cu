@@ -59,7 +59,7 @@ constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
 
 // ----------------------------------------------------------------- conv
 struct ConvGeom {
-  int B, H, W, Ci, Co, P, fresh_halo;
+  int B, H, W, Ci, Co, P, fresh_halo, zero_halo;
 };
 
 template <typename T>
@@ -84,7 +84,8 @@ conv_simt_kernel(const T *__restrict__ x, const T *__restrict__ stale, const T *
   for (int tap = 0; tap < 9; ++tap) {
     const int dy = tap / 3, dx = tap % 3;
     const int r = h_ + dy - 1, c = w_ + dx - 1;
-    const bool in_img = m_ok && r >= 0 && r < g.H && c >= 0 && c < g.W;
+    const bool in_img = m_ok && r >= 0 && r < g.H && c >= 0 && c < g.W &&
+                        !(g.zero_halo && (r < lo || r >= hi));
     const T *src = (g.fresh_halo || (r >= lo && r < hi)) ? x : stale;
     const T *arow = src + (((size_t)b_ * g.H + (in_img ? r : 0)) * g.W + (in_img ? c : 0)) * g.Ci;
     const T *wrow = w + ((size_t)(co_l < g.Co ? co_l : 0) * 9 + tap) * g.Ci;
@@ -230,11 +231,13 @@ __global__ void __launch_bounds__(NT) attn_simt_kernel(AttnArgs a) {
     m_i[i] = -INFINITY;
     l_i[i] = 0.f;
   }
-  for (int kv0 = 0; kv0 < a.Nkv; kv0 += AK) {
+  // band-local (naive patches): only the band's own keys
+  const int k_begin = a.band_local ? kv_lo : 0, k_end = a.band_local ? kv_hi : a.Nkv;
+  for (int kv0 = k_begin; kv0 < k_end; kv0 += AK) {
     __syncthreads();  // previous tile fully consumed
     {
       const int kv = kv0 + lr;
-      const bool ok = kv < a.Nkv;
+      const bool ok = kv < k_end;
       const bool fresh = (KVs == nullptr) || (kv >= kv_lo && kv < kv_hi);
       const T *src = (fresh ? KVf : KVs) + ((size_t)b * a.Nkv + (ok ? kv : 0)) * 2 * a.C +
                      head * AD + lq * 16;
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(NT) attn_simt_kernel(AttnArgs a) {
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      if (kv0 + tx + 16 * j >= a.Nkv)
+      if (kv0 + tx + 16 * j >= k_end)
 #pragma unroll
         for (int i = 0; i < 4; ++i) s[i][j] = -INFINITY;
 #pragma unroll
@@ -321,8 +324,9 @@ __global__ void __launch_bounds__(NT) attn_simt_kernel(AttnArgs a) {
 
 cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *stale,
                              const void *w, const float *bias, void *y, cudaStream_t s) {
-  const int fresh_halo = (d.first_layer || stale == nullptr || stale == x) ? 1 : 0;
-  ConvGeom g{d.B, d.H, d.W, d.C_in, d.C_out, d.P, fresh_halo};
+  const int fresh_halo = (d.halo == DPP_HALO_FRESH || stale == nullptr || stale == x) ? 1 : 0;
+  const int zero_halo = d.halo == DPP_HALO_ZERO ? 1 : 0;
+  ConvGeom g{d.B, d.H, d.W, d.C_in, d.C_out, d.P, fresh_halo, zero_halo};
   const void *st = fresh_halo ? x : stale;
   const long long M = (long long)d.B * d.H * d.W;
   dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((d.C_out + BN - 1) / BN));

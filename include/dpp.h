@@ -81,29 +81,43 @@ typedef enum {
 
 typedef enum { DPP_F32 = 0, DPP_BF16 = 1 } dpp_dtype;
 
-/* 3x3 conv, stride 1, zero padding 1, C_in -> C_out.
- * first_layer: the conv_in flag of the conv wrapper (is_first_layer); the
- * input latent is identical on every device, so the halo is fresh and
- * stale_prev is ignored. */
+/* Where a band's conv reads the input rows just outside the band (its halo):
+ *   DPP_HALO_STALE  displaced patch parallelism: from stale_prev (the
+ *                   previous step), or fresh for the synchronous step;
+ *   DPP_HALO_FRESH  the conv_in flag of the conv wrapper (is_first_layer):
+ *                   the input latent is identical on every device, so the
+ *                   halo is fresh and stale_prev is ignored;
+ *   DPP_HALO_ZERO   naive patch parallelism (every band an image of its own,
+ *                   zero-padded at its edges: the seam baseline of the
+ *                   DistriFusion notes, Introduction para. 3). */
+typedef enum { DPP_HALO_STALE = 0, DPP_HALO_FRESH = 1, DPP_HALO_ZERO = 2 } dpp_halo;
+
+/* 3x3 conv, stride 1, zero padding 1, C_in -> C_out; halo: a dpp_halo. */
 typedef struct {
   int B, H, W, C_in, C_out, P;
   dpp_dtype dtype;
-  int first_layer;
+  int halo;
 } dpp_conv_desc;
 
-/* GroupNorm over [B, H, W, C] with G groups of C/G consecutive channels. */
+/* GroupNorm over [B, H, W, C] with G groups of C/G consecutive channels.
+ * band_local != 0: naive patch parallelism -- each band's statistics over
+ * its own rows only (stats_prev is ignored). */
 typedef struct {
   int B, H, W, C, G, P;
   float eps;
   dpp_dtype dtype;
+  int band_local;
 } dpp_gn_desc;
 
 /* Attention over an H x W token grid (N = H*W), C = heads * head_dim.
- * n_ctx / c_ctx: text-context length and width (cross-attention only). */
+ * n_ctx / c_ctx: text-context length and width (cross-attention only).
+ * band_local != 0 (self-attention): naive patch parallelism -- a band's
+ * queries attend over its own tokens only (kv_prev is ignored). */
 typedef struct {
   int B, H, W, C, heads, head_dim, P;
   int n_ctx, c_ctx;
   dpp_dtype dtype;
+  int band_local;
 } dpp_attn_desc;
 
 /* ---------------------------------------------------------------------------
@@ -119,7 +133,9 @@ typedef struct {
  *   w                : [C_out, 3, 3, C_in] (torch [C_out, C_in, 3, 3] in
  *                      channels_last memory), desc->dtype.
  *   bias             : [C_out] fp32 or NULL.
- * Requires H % P == 0, C_in and C_out multiples of 8 (bf16) / 4 (f32).
+ * Requires H % P == 0, C_in and C_out multiples of 8 (bf16) / 4 (f32),
+ * halo one of the dpp_halo values.  With DPP_HALO_ZERO the rows outside
+ * the band read as zero (naive patches); with DPP_HALO_FRESH as x.
  * y must not overlap x or stale_prev.
  * ------------------------------------------------------------------------- */
 dpp_status dpp_conv3x3(const dpp_conv_desc *desc, const void *x, const void *stale_prev,

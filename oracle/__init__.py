@@ -42,13 +42,16 @@ from .displaced import (  # noqa: F401
     composite,
     conv3x3,
     displaced_conv3x3,
+    naive_conv3x3,
     groupnorm,
     groupnorm_partials,
     displaced_groupnorm,
+    naive_groupnorm,
     attention_heads,
     linear,
     kv_state,
     displaced_self_attention,
+    naive_self_attention,
     cross_attention,
     cfg_combine,
     rel_mae,

@@ -119,6 +119,23 @@ def displaced_conv3x3(F, S, Wt, bias, P, out_rows=None, first_layer=False):
     return out
 
 
+def naive_conv3x3(F, Wt, bias, P, out_rows=None):
+    """Naive patch parallelism ([DF-notes] Introduction para. 3): band p is
+    convolved as an image of its own, so the rows just outside the band read
+    as zero (zero padding at every band edge) -- no stale buffer, and the
+    seams the method exists to remove.  Returns ``[B, len(out_rows), W, C_out]``."""
+    B, H, W, _ = F.shape
+    rows = range(H) if out_rows is None else list(out_rows)
+    out = np.zeros((B, len(rows), W, Wt.shape[0]))
+    for k, h in enumerate(rows):
+        lo, hi = patch_rows(H, P, patch_of_row(h, H, P))
+        src = [F[:, r] if lo <= r < hi else None for r in (h - 1, h, h + 1)]
+        out[:, k] = _conv_row(src, Wt, W)
+        if bias is not None:
+            out[:, k] += bias
+    return out
+
+
 # --------------------------------------------------------------------------
 # GroupNorm (DistriGroupNorm, [DF-guide] 归一化层拆分)
 # --------------------------------------------------------------------------
@@ -164,6 +181,18 @@ def displaced_groupnorm(F, S, G, eps, gamma, beta, P, bands=None):
     for p in (range(P) if bands is None else bands):
         lo, hi = patch_rows(H, P, p)
         out[:, lo:hi] = groupnorm(composite(F, S, P, p), G, eps, gamma, beta)[:, lo:hi]
+    return out
+
+
+def naive_groupnorm(F, G, eps, gamma, beta, P):
+    """Naive patch parallelism ([DF-notes] Introduction para. 3: every band
+    generated on its own, no interaction): band p normalised with the
+    statistics of its own rows only, i.e. groupnorm of the band alone."""
+    B, H, W, C = F.shape
+    out = np.zeros((B, H, W, C))
+    for p in range(P):
+        lo, hi = patch_rows(H, P, p)
+        out[:, lo:hi] = groupnorm(F[:, lo:hi], G, eps, gamma, beta)
     return out
 
 
@@ -220,6 +249,21 @@ def displaced_self_attention(F, S, Wq, Wk, Wv, Wo, heads, P, queries=None):
             Q = linear(F[b, qs[sel]], Wq)
             O = attention_heads(Q, linear(Z, Wk), linear(Z, Wv), heads)
             out[b, sel] = linear(O, Wo)
+    return out
+
+
+def naive_self_attention(F, Wq, Wk, Wv, Wo, heads, P):
+    """Naive patch parallelism ([DF-notes] Introduction para. 3): band p's
+    queries attend over the band's own tokens only -- self-attention of each
+    band as a sequence of its own.  Returns ``[B, N, C]``."""
+    B, N, C = F.shape
+    out = np.zeros((B, N, Wo.shape[0]))
+    for p in range(P):
+        lo, hi = patch_rows(N, P, p)
+        for b in range(B):
+            X = F[b, lo:hi]
+            O = attention_heads(linear(X, Wq), linear(X, Wk), linear(X, Wv), heads)
+            out[b, lo:hi] = linear(O, Wo)
     return out
 
 

@@ -40,29 +40,30 @@ def assert_rms_close(got, want, rel, what=""):
 
 
 # ---------------------------------------------------------------- conv
-def conv(x, stale, w, bias, P, first_layer=False, stream=None):
-    """x, stale: [B,H,W,Ci] (device or CPU); w: [Co,Ci,3,3] torch order."""
+def conv(x, stale, w, bias, P, halo=dpp.DPP_HALO_STALE, stream=None):
+    """x, stale: [B,H,W,Ci] (device or CPU); w: [Co,Ci,3,3] torch order;
+    halo: a DPP_HALO_* value."""
     x = cuda(x)
     stale = cuda(stale) if stale is not None and stale.device.type == "cpu" else stale
     B, H, W, Ci = x.shape
     Co = w.shape[0]
     wd = cuda(w.permute(0, 2, 3, 1))  # [Co,3,3,Ci]
     y = torch.empty((B, H, W, Co), dtype=x.dtype, device="cuda")
-    d = dpp.dpp_conv_desc(B, H, W, Ci, Co, P, CODES[x.dtype], int(first_layer))
+    d = dpp.dpp_conv_desc(B, H, W, Ci, Co, P, CODES[x.dtype], int(halo))
     dpp.dpp_conv3x3(d, x, stale, wd, cuda(bias), y, stream=stream)
     return y
 
 
 # ------------------------------------------------------------ groupnorm
-def gn_desc(x, G, eps, P):
+def gn_desc(x, G, eps, P, band_local=False):
     B, H, W, C = x.shape
-    return dpp.dpp_gn_desc(B, H, W, C, G, P, eps, CODES[x.dtype])
+    return dpp.dpp_gn_desc(B, H, W, C, G, P, eps, CODES[x.dtype], int(band_local))
 
 
-def groupnorm(x, stats_prev, G, eps, gamma, beta, P, y=None, stream=None):
+def groupnorm(x, stats_prev, G, eps, gamma, beta, P, y=None, stream=None, band_local=False):
     """Returns (y, stats_next) as device tensors."""
     x = cuda(x)
-    d = gn_desc(x, G, eps, P)
+    d = gn_desc(x, G, eps, P, band_local)
     B = x.shape[0]
     stats_next = torch.empty((P, B, G, 2), dtype=torch.float32, device="cuda")
     nws = dpp.dpp_groupnorm_workspace_bytes(d)
@@ -102,17 +103,18 @@ def groupnorm_apply(x, stats_prev, gn_sums, G, eps, gamma, beta, P, y=None, stre
 
 
 # ------------------------------------------------------------ attention
-def attn_desc(x, H, W, heads, P, n_ctx=0, c_ctx=0):
+def attn_desc(x, H, W, heads, P, n_ctx=0, c_ctx=0, band_local=False):
     B, N, C = x.shape
     assert N == H * W
-    return dpp.dpp_attn_desc(B, H, W, C, heads, C // heads, P, n_ctx, c_ctx, CODES[x.dtype])
+    return dpp.dpp_attn_desc(B, H, W, C, heads, C // heads, P, n_ctx, c_ctx, CODES[x.dtype],
+                             int(band_local))
 
 
-def self_attn(x, wts, kv_prev, H, W, heads, P, stream=None):
+def self_attn(x, wts, kv_prev, H, W, heads, P, stream=None, band_local=False):
     """Returns (y, kv_next) as device tensors."""
     x = cuda(x)
     B, N, C = x.shape
-    d = attn_desc(x, H, W, heads, P)
+    d = attn_desc(x, H, W, heads, P, band_local=band_local)
     kv_next = torch.empty((B, N, 2, C), dtype=KV_DTYPE[x.dtype], device="cuda")
     y = torch.empty_like(x)
     nws = dpp.dpp_self_attn_workspace_bytes(d)

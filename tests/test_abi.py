@@ -55,7 +55,7 @@ def test_status_strings_and_version():
 
 
 def conv(**kw):
-    d = dict(B=1, H=8, W=8, C_in=16, C_out=16, P=2, dtype=dpp.DPP_BF16, first_layer=0)
+    d = dict(B=1, H=8, W=8, C_in=16, C_out=16, P=2, dtype=dpp.DPP_BF16, halo=0)
     d.update(kw)
     return dpp.dpp_conv_desc(**d)
 
@@ -65,6 +65,7 @@ def conv(**kw):
     (dict(C_in=12), {}, dpp.DPP_ERR_INVALID_ARG),         # bf16 needs C % 8 == 0
     (dict(P=0), {}, dpp.DPP_ERR_INVALID_ARG),
     (dict(dtype=5), {}, dpp.DPP_ERR_INVALID_ARG),
+    (dict(halo=3), {}, dpp.DPP_ERR_INVALID_ARG),          # not a dpp_halo value
     ({}, dict(x=0), dpp.DPP_ERR_INVALID_ARG),             # null input
     ({}, dict(x=A + 8), dpp.DPP_ERR_ALIGN),
     ({}, dict(y=A + 64), dpp.DPP_ERR_ALIAS),              # output overlaps input

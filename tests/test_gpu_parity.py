@@ -141,7 +141,7 @@ def test_conv_reads_only_halo_rows_of_stale(cuda_device):
 def test_conv_first_layer_ignores_stale(cuda_device):
     F, S = draw((1, 8, 16, 32), 5, BF16), draw((1, 8, 16, 32), 6, BF16)
     Wt = wl.conv_weight(32, 32, 7, "bf16")
-    y = G.conv(F, S, Wt, None, 4, first_layer=True)
+    y = G.conv(F, S, Wt, None, 4, halo=G.dpp.DPP_HALO_FRESH)
     assert torch.equal(y, G.conv(F, None, Wt, None, 4))
 
 

@@ -115,6 +115,18 @@ def _refresh_off_by_one(fresh, stale, P, patch_mask=None, axis=1):
     return out
 
 
+def _naive_conv_reads_neighbours(F, Wt, bias, P, out_rows=None):
+    return od.conv3x3(F, Wt, bias, out_rows)
+
+
+def _naive_gn_image_statistics(F, G, eps, gamma, beta, P):
+    return od.groupnorm(F, G, eps, gamma, beta)
+
+
+def _naive_attention_all_keys(F, Wq, Wk, Wv, Wo, heads, P):
+    return od.displaced_self_attention(F, F, Wq, Wk, Wv, Wo, heads, P)
+
+
 MUTATIONS = {
     "conv_taps_transposed": [("_conv_row", _conv_row_transposed)],
     "conv_halo_fresh": [("displaced_conv3x3", _displaced_conv_fresh_halo)],
@@ -128,6 +140,9 @@ MUTATIONS = {
     "cfg_wrong_base": [("cfg_combine", _cfg_wrong_base)],
     "rel_mae_by_cond": [("rel_mae", _rel_mae_by_cond)],
     "refresh_off_by_one": [("refresh_stale", _refresh_off_by_one)],
+    "naive_conv_reads_neighbours": [("naive_conv3x3", _naive_conv_reads_neighbours)],
+    "naive_gn_image_statistics": [("naive_groupnorm", _naive_gn_image_statistics)],
+    "naive_attention_all_keys": [("naive_self_attention", _naive_attention_all_keys)],
 }
 
 

@@ -430,3 +430,68 @@ def test_refresh_matches_slicing():
         got = oracle.refresh_stale(fresh.numpy(), stale.numpy(), 4, mask)
         assert np.array_equal(got, want.numpy())
     assert np.array_equal(oracle.refresh_stale(fresh.numpy(), stale.numpy(), 4), fresh.numpy())
+
+
+# ------------------------------------------------- naive patch parallelism
+# The seam baseline ([DF-notes] Introduction para. 3): every band on its own.
+
+@pytest.mark.parametrize("B,H,W,Ci,Co,P", [(1, 6, 5, 3, 2, 3), (2, 4, 3, 2, 3, 2)])
+def test_naive_conv_bruteforce_tiny(B, H, W, Ci, Co, P):
+    """Per-element loops: the input rows outside the output row's band count
+    as zero, exactly like the image border."""
+    F, Wt, bias = rnd(B, H, W, Ci), rnd(Co, Ci, 3, 3), rnd(Co)
+    want = np.zeros((B, H, W, Co))
+    Hp = H // P
+    for b, h, w, o in itertools.product(range(B), range(H), range(W), range(Co)):
+        lo, hi = (h // Hp) * Hp, (h // Hp + 1) * Hp
+        acc = bias[o]
+        for i, dy, dx in itertools.product(range(Ci), range(3), range(3)):
+            r, c = h + dy - 1, w + dx - 1
+            if lo <= r < hi and 0 <= c < W:
+                acc += Wt[o, i, dy, dx] * F[b, r, c, i]
+        want[b, h, w, o] = acc
+    np.testing.assert_allclose(oracle.naive_conv3x3(F, Wt, bias, P), want, rtol=0, atol=1e-12)
+
+
+def test_naive_ops_with_one_band_are_the_full_layers():
+    X, Wt = rnd(2, 6, 5, 8), rnd(4, 8, 3, 3)
+    np.testing.assert_allclose(oracle.naive_conv3x3(X, Wt, None, 1), torch_conv_nhwc(X, Wt),
+                               rtol=0, atol=1e-12)
+    g, bt = rnd(8), rnd(8)
+    np.testing.assert_allclose(oracle.naive_groupnorm(X, 4, 1e-5, g, bt, 1),
+                               torch_gn_nhwc(X, 4, 1e-5, g, bt), rtol=0, atol=1e-12)
+    F = rnd(2, 8, 8)
+    Ws = [rnd(8, 8) / math.sqrt(8) for _ in range(4)]
+    out = oracle.naive_self_attention(F, *Ws, 2, 1)
+    for b in range(2):
+        np.testing.assert_allclose(out[b], torch_mha(F[b], F[b], *Ws, 2), rtol=0, atol=1e-12)
+
+
+def test_naive_groupnorm_is_torch_group_norm_of_each_band():
+    X, g, bt = rnd(2, 8, 3, 12), rnd(12), rnd(12)
+    out = oracle.naive_groupnorm(X, 3, 1e-5, g, bt, 4)
+    for p in range(4):
+        np.testing.assert_allclose(out[:, 2 * p:2 * p + 2],
+                                   torch_gn_nhwc(X[:, 2 * p:2 * p + 2], 3, 1e-5, g, bt),
+                                   rtol=0, atol=1e-12)
+    # without affine every (image, band, group) has mean 0 and variance 1
+    y = oracle.naive_groupnorm(X, 3, 0.0, None, None, 4).reshape(2, 4, 2 * 3, 3, 4)
+    np.testing.assert_allclose(y.mean(axis=(2, 4)), 0.0, atol=1e-12)
+    np.testing.assert_allclose(y.var(axis=(2, 4)), 1.0, atol=1e-9)
+
+
+def test_naive_self_attention_is_band_local_attention():
+    B, N, C, heads, P = 2, 12, 8, 2, 3
+    F = rnd(B, N, C)
+    Ws = [rnd(C, C) / math.sqrt(C) for _ in range(4)]
+    out = oracle.naive_self_attention(F, *Ws, heads, P)
+    Np = N // P
+    for b, p in itertools.product(range(B), range(P)):
+        X = F[b, p * Np:(p + 1) * Np]
+        np.testing.assert_allclose(out[b, p * Np:(p + 1) * Np], torch_mha(X, X, *Ws, heads),
+                                   rtol=0, atol=1e-12)
+    # tokens outside a band never reach its output
+    G2 = F.copy()
+    G2[:, Np:] += 5.0
+    np.testing.assert_allclose(oracle.naive_self_attention(G2, *Ws, heads, P)[:, :Np],
+                               out[:, :Np], rtol=0, atol=1e-12)
