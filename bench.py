@@ -302,13 +302,25 @@ class Step:
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
-    def h2d(self):
-        s = self.stream
-        self.x.copy_(self.host_x, non_blocking=True)
-        self.xa.copy_(self.host_xa, non_blocking=True)
-        self.ctx.copy_(self.host_ctx, non_blocking=True)
-        self.u.copy_(self.host_u, non_blocking=True)
-        self.c.copy_(self.host_c, non_blocking=True)
+    # The step's inputs copied in and results copied out each end-to-end step;
+    # two device sets, so one step's copies overlap the other set's compute.
+    IO = ("x", "xa", "ctx", "u", "c", "y2", "yc", "cfg_out", "sums")
+
+    def make_io_sets(self):
+        self._sets = [{n: getattr(self, n) for n in self.IO},
+                      {n: torch.empty_like(getattr(self, n)) for n in self.IO}]
+
+    def select(self, i):
+        for n, t in self._sets[i].items():
+            setattr(self, n, t)
+
+    def h2d(self, stream):
+        with torch.cuda.stream(stream):
+            self.x.copy_(self.host_x, non_blocking=True)
+            self.xa.copy_(self.host_xa, non_blocking=True)
+            self.ctx.copy_(self.host_ctx, non_blocking=True)
+            self.u.copy_(self.host_u, non_blocking=True)
+            self.c.copy_(self.host_c, non_blocking=True)
         return sum(t.numel() * t.element_size() for t in
                    (self.host_x, self.host_xa, self.host_ctx, self.host_u, self.host_c))
 
@@ -317,9 +329,10 @@ class Step:
                          for t in (self.y2, self.yc, self.cfg_out, self.sums)]
         return sum(t.numel() * t.element_size() for t in self.out_host)
 
-    def d2h(self):
-        for h, d in zip(self.out_host, (self.y2, self.yc, self.cfg_out, self.sums)):
-            h.copy_(d, non_blocking=True)
+    def d2h(self, stream):
+        with torch.cuda.stream(stream):
+            for h, d in zip(self.out_host, (self.y2, self.yc, self.cfg_out, self.sums)):
+                h.copy_(d, non_blocking=True)
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -529,14 +542,39 @@ def main():
         torch.cuda.synchronize(dev)
         if pg:
             pg.barrier()
+        # Every step copies its inputs in from pinned host memory and its
+        # results out, all inside the timed region; with two device sets the
+        # copies of one step run on a copy stream while the other set's step
+        # computes (step k+1's inputs are copied once step k-1, the last user
+        # of that set, is done; step k's results once step k is done).
+        step.make_io_sets()
+        cs = torch.cuda.Stream(dev)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        for _ in range(K):
-            bi = step.h2d()
+        cs.wait_stream(s)
+        e0.record(cs)
+        step.select(0)
+        bi = step.h2d(cs)
+        in_ready[0].record(cs)
+        for k in range(K):
+            i, j = k % 2, 1 - k % 2
+            step.select(i)
+            s.wait_event(in_ready[i])
             step.run()
-            step.d2h()
-        e1.record(s)
+            done[i].record(s)
+            if k + 1 < K:
+                if k >= 1:
+                    cs.wait_event(done[j])
+                step.select(j)
+                step.h2d(cs)
+                in_ready[j].record(cs)
+                step.select(i)
+            cs.wait_event(done[i])
+            step.d2h(cs)
+        e1.record(cs)
         torch.cuda.synchronize(dev)
+        step.select(0)
         e2e_ms = e0.elapsed_time(e1)
         if pg:
             t = torch.tensor([e2e_ms], device=dev)
