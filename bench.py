@@ -45,6 +45,9 @@ import workloads as wl  # noqa: E402
 
 METRIC = "displaced-patch conv/attn TFLOP/s, GroupNorm GB/s; % of B300 roofline"
 WORKLOAD = "sdxl_3840_cfg"
+# adaptive switching controller of the end-to-end loop: relative-drop and
+# rise tolerances and patience (the pages give no values)
+SWITCH_FLAT_TOL, SWITCH_RISE_TOL, SWITCH_PATIENCE = 0.02, 0.05, 2
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -537,6 +540,7 @@ def main():
     # end to end: pinned host inputs -> device, step, results -> host
     bi = bo = 0
     e2e_val = None
+    stages = []
     if K > 0:
         bo = step.alloc_d2h()
         torch.cuda.synchronize(dev)
@@ -557,12 +561,28 @@ def main():
         step.select(0)
         bi = step.h2d(cs)
         in_ready[0].record(cs)
+        # The sampler's side of each step: once a step's results are on the
+        # host, its discrepancy (rel-MAE from the guidance sums) goes to the
+        # adaptive switching controller, which names the stage of the steps
+        # to come.  The host waits for step k-1's results only after step k
+        # is queued, so the device never idles on it.
+        sw = dpp.dpp_switch_state()
+        dpp.dpp_switch_init(sw, SWITCH_FLAT_TOL, SWITCH_RISE_TOL, SWITCH_PATIENCE)
+        stages, out_copied = [], torch.cuda.Event()
+
+        def observe():
+            out_copied.synchronize()
+            h = step.out_host[3]
+            stages.append(dpp.dpp_switch_update(sw, float(h[0] / h[1])))
+
         for k in range(K):
             i, j = k % 2, 1 - k % 2
             step.select(i)
             s.wait_event(in_ready[i])
             step.run()
             done[i].record(s)
+            if k >= 1:
+                observe()
             if k + 1 < K:
                 if k >= 1:
                     cs.wait_event(done[j])
@@ -572,6 +592,8 @@ def main():
                 step.select(i)
             cs.wait_event(done[i])
             step.d2h(cs)
+            out_copied.record(cs)
+        observe()
         e1.record(cs)
         torch.cuda.synchronize(dev)
         step.select(0)
@@ -611,7 +633,7 @@ def main():
             "ops": ops,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
-                    "d2h_bytes_per_step": bo},
+                    "d2h_bytes_per_step": bo, "switch_stages": stages},
             "gpu_launches": launches,
             "clocks": clocks,
         }

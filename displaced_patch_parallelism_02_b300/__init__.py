@@ -66,6 +66,16 @@ class dpp_attn_desc(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("band_local", ctypes.c_int)]
 
 
+class dpp_switch_state(ctypes.Structure):
+    _fields_ = [("flat_tol", ctypes.c_double), ("rise_tol", ctypes.c_double),
+                ("patience", ctypes.c_int), ("stage", ctypes.c_int), ("run", ctypes.c_int),
+                ("steps", ctypes.c_int), ("prev", ctypes.c_double), ("min_d", ctypes.c_double)]
+
+
+DPP_STAGE_WARMUP = 0
+DPP_STAGE_PARALLEL = 1
+DPP_STAGE_FULLY_CONNECTING = 2
+
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
 _st = ctypes.c_int
@@ -95,6 +105,9 @@ _SIGNATURES = {
     "dpp_version": (ctypes.c_int, []),
     "dpp_launch_count": (ctypes.c_uint64, []),
     "dpp_set_attn_core_events": (None, [_vp, _vp]),
+    "dpp_switch_init": (None, [ctypes.POINTER(dpp_switch_state), ctypes.c_double,
+                               ctypes.c_double, ctypes.c_int]),
+    "dpp_switch_update": (ctypes.c_int, [ctypes.POINTER(dpp_switch_state), ctypes.c_double]),
 }
 
 for _name, (_res, _args) in _SIGNATURES.items():
@@ -145,6 +158,15 @@ def dpp_set_attn_core_events(start, stop) -> None:
     """start/stop: torch.cuda.Event (recorded by the library) or None."""
     lib.dpp_set_attn_core_events(None if start is None else start.cuda_event,
                                  None if stop is None else stop.cuda_event)
+
+
+def dpp_switch_init(state: dpp_switch_state, flat_tol: float, rise_tol: float,
+                    patience: int) -> None:
+    lib.dpp_switch_init(ctypes.byref(state), float(flat_tol), float(rise_tol), int(patience))
+
+
+def dpp_switch_update(state: dpp_switch_state, d: float) -> int:
+    return lib.dpp_switch_update(ctypes.byref(state), float(d))
 
 
 def dpp_device_status(stream=None) -> int:

@@ -298,6 +298,35 @@ size_t dpp_cfg_workspace_bytes(size_t n);
 dpp_status dpp_refresh_stale(const void *fresh, void *stale, size_t outer, size_t rows,
                              size_t row_bytes, int P, uint64_t patch_mask, dpp_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * Adaptive parallelism switching (the Hydiff summaries: gist.science,
+ * section 自适应并行切换; Avetisyan, "Адаптивное переключение").  Host-side
+ * state machine over the per-step denoising discrepancy d (rel-MAE of the
+ * conditional vs the unconditional noise estimate: sums3[0] / sums3[1] of
+ * dpp_cfg_combine).  Three stages: warm-up (serial) until tau1, where the
+ * decline of d flattens; parallel until tau2, where d starts rising; fully
+ * connecting (serial) to the end.  The pages fix no thresholds:
+ *   tau1: for `patience` consecutive steps the relative drop
+ *         (d_prev - d) / d_prev is below flat_tol (a rise counts as flat);
+ *   tau2: for `patience` consecutive steps d exceeds the lowest d of the
+ *         parallel stage by more than the fraction rise_tol.
+ * dpp_switch_update feeds one step's d and returns the stage the next step
+ * runs in; NaN or negative d changes nothing.  Host only: no GPU work, no
+ * allocation, no global state.
+ * ------------------------------------------------------------------------- */
+enum { DPP_STAGE_WARMUP = 0, DPP_STAGE_PARALLEL = 1, DPP_STAGE_FULLY_CONNECTING = 2 };
+typedef struct {
+  double flat_tol, rise_tol;
+  int patience;
+  int stage;   /* DPP_STAGE_* */
+  int run;     /* consecutive steps the current stage's exit condition has held */
+  int steps;   /* steps observed */
+  double prev; /* last d */
+  double min_d; /* lowest d in the parallel stage */
+} dpp_switch_state;
+void dpp_switch_init(dpp_switch_state *state, double flat_tol, double rise_tol, int patience);
+int dpp_switch_update(dpp_switch_state *state, double d);
+
 /* Reads and clears the device status word written by bounded waits
  * (DPP_OK or DPP_ERR_TIMEOUT).  Synchronises `stream`. */
 dpp_status dpp_device_status(dpp_stream stream);

@@ -56,4 +56,8 @@ from .displaced import (  # noqa: F401
     cfg_combine,
     rel_mae,
     refresh_stale,
+    switch_stages,
+    WARMUP,
+    PARALLEL,
+    FULLY_CONNECTING,
 )

@@ -324,3 +324,67 @@ def refresh_stale(fresh, stale, P, patch_mask=None, axis=1):
         idx[axis] = slice(lo, hi)
         out[tuple(idx)] = fresh[tuple(idx)]
     return out
+
+
+# --------------------------------------------------------------------------
+# Adaptive parallelism switching ([Hydiff-zh] 自适应并行切换; [Hydiff-ru]
+# Адаптивное переключение)
+# --------------------------------------------------------------------------
+
+WARMUP, PARALLEL, FULLY_CONNECTING = 0, 1, 2
+
+
+def switch_stages(ds, flat_tol, rise_tol, patience):
+    """Stage each denoising step runs in, read off the discrepancy series.
+
+    [Hydiff-zh] splits the sampling run T -> 0 into a warm-up stage (T -> tau1,
+    branches run serially), a parallel stage (tau1 -> tau2) and a fully
+    connecting stage (tau2 -> 0, serial again); tau1 is where the decline of
+    the discrepancy flattens and tau2 where it starts rising, both found from
+    the live curve.  The pages give no numbers, so:
+
+      tau1 = the first observation t >= patience at which each of the last
+             ``patience`` relative drops (d[j-1] - d[j]) / d[j-1] is below
+             flat_tol (a zero d[j-1] counts as drop 0);
+      tau2 = the first observation t >= tau1 + patience at which each of the
+             last ``patience`` values d[j] (j > tau1) is above
+             (1 + rise_tol) * min(d[tau1..j]).
+
+    Returns, for every entry of ``ds``, the stage after seeing it (the stage
+    the next step runs in).  An entry that is NaN or negative carries no
+    information: it is skipped and repeats the stage before it.
+    """
+    patience = max(1, int(patience))
+    valid = [i for i, d in enumerate(ds) if d >= 0.0]  # False for NaN too
+    v = [float(ds[i]) for i in valid]
+
+    def drop(j):
+        return (v[j - 1] - v[j]) / v[j - 1] if v[j - 1] > 0.0 else 0.0
+
+    tau1 = None
+    for t in range(patience, len(v)):
+        if all(drop(j) < flat_tol for j in range(t - patience + 1, t + 1)):
+            tau1 = t
+            break
+    tau2 = None
+    if tau1 is not None:
+        for t in range(tau1 + patience, len(v)):
+            if all(v[j] > min(v[tau1:j + 1]) * (1.0 + rise_tol)
+                   for j in range(t - patience + 1, t + 1)):
+                tau2 = t
+                break
+
+    def stage_at(t):
+        if tau2 is not None and t >= tau2:
+            return FULLY_CONNECTING
+        if tau1 is not None and t >= tau1:
+            return PARALLEL
+        return WARMUP
+
+    out, last, k = [], WARMUP, 0
+    for i in range(len(ds)):
+        if k < len(valid) and valid[k] == i:
+            last = stage_at(k)
+            k += 1
+        out.append(last)
+    return out

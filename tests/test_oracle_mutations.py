@@ -127,6 +127,39 @@ def _naive_attention_all_keys(F, Wq, Wk, Wv, Wo, heads, P):
     return od.displaced_self_attention(F, F, Wq, Wk, Wv, Wo, heads, P)
 
 
+def _switch_variant(absolute_drop=False, rise_vs_previous=False, short_window=False):
+    def stages(ds, flat_tol, rise_tol, patience):
+        patience = max(1, int(patience))
+        v = [float(x) for x in ds if x >= 0.0]
+        w = patience - 1 if short_window and patience > 1 else patience
+
+        def drop(j):
+            if absolute_drop:
+                return v[j - 1] - v[j]
+            return (v[j - 1] - v[j]) / v[j - 1] if v[j - 1] > 0.0 else 0.0
+
+        def ref(j, tau1):
+            return v[j - 1] if rise_vs_previous else min(v[tau1:j + 1])
+
+        tau1 = next((t for t in range(w, len(v))
+                     if all(drop(j) < flat_tol for j in range(t - w + 1, t + 1))), None)
+        tau2 = None
+        if tau1 is not None:
+            tau2 = next((t for t in range(tau1 + w, len(v))
+                         if all(v[j] > ref(j, tau1) * (1.0 + rise_tol)
+                                for j in range(t - w + 1, t + 1))), None)
+        out = [2 if tau2 is not None and t >= tau2 else 1 if tau1 is not None and t >= tau1
+               else 0 for t in range(len(v))]
+        res, k, last = [], 0, 0
+        for x in ds:
+            if x >= 0.0:
+                last = out[k]
+                k += 1
+            res.append(last)
+        return res
+    return stages
+
+
 MUTATIONS = {
     "conv_taps_transposed": [("_conv_row", _conv_row_transposed)],
     "conv_halo_fresh": [("displaced_conv3x3", _displaced_conv_fresh_halo)],
@@ -143,6 +176,9 @@ MUTATIONS = {
     "naive_conv_reads_neighbours": [("naive_conv3x3", _naive_conv_reads_neighbours)],
     "naive_gn_image_statistics": [("naive_groupnorm", _naive_gn_image_statistics)],
     "naive_attention_all_keys": [("naive_self_attention", _naive_attention_all_keys)],
+    "switch_absolute_drop": [("switch_stages", _switch_variant(absolute_drop=True))],
+    "switch_rise_vs_previous": [("switch_stages", _switch_variant(rise_vs_previous=True))],
+    "switch_short_window": [("switch_stages", _switch_variant(short_window=True))],
 }
 
 

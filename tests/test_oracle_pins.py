@@ -495,3 +495,75 @@ def test_naive_self_attention_is_band_local_attention():
     G2[:, Np:] += 5.0
     np.testing.assert_allclose(oracle.naive_self_attention(G2, *Ws, heads, P)[:, :Np],
                                out[:, :Np], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------ adaptive switching
+# Worked by hand (flat_tol 0.05, rise_tol 0.10, patience 2):
+#   relative drops   d1 .5, d2 .5, d3 .025 (flat, run 1), d4 .23 (reset),
+#                    d5 .033 (flat, run 1), d6 .0069 (flat, run 2) -> tau1 = 6;
+#   parallel, min 1.44: d7 1.60 > 1.584 (run 1); d8 1.40 new min (reset);
+#                    d9 1.50 < 1.54 (reset); d10 1.55 > 1.54 (run 1);
+#                    d11 1.56 > 1.54 (run 2) -> tau2 = 11; d12 falls, no way back.
+SWITCH_SERIES = [8.0, 4.0, 2.0, 1.95, 1.5, 1.45, 1.44, 1.60, 1.40, 1.50, 1.55, 1.56, 1.2]
+SWITCH_STAGES = [0, 0, 0, 0, 0, 0, 1, 1, 1, 1, 1, 2, 2]
+
+
+def test_switch_worked_example():
+    assert oracle.switch_stages(SWITCH_SERIES, 0.05, 0.10, 2) == SWITCH_STAGES
+
+
+@pytest.mark.parametrize("patience", [1, 2, 3, 5])
+def test_switch_geometric_decline_closed_form(patience):
+    # d_t = 10 r^t has the constant relative drop 1 - r: flat from the first
+    # step when 1 - r < flat_tol (tau1 = patience, then it never rises),
+    # never flat otherwise.
+    slow = [10.0 * 0.99 ** t for t in range(30)]
+    assert oracle.switch_stages(slow, 0.02, 0.01, patience) == \
+        [0] * patience + [1] * (30 - patience)
+    fast = [10.0 * 0.9 ** t for t in range(30)]
+    assert oracle.switch_stages(fast, 0.02, 0.01, patience) == [0] * 30
+
+
+@pytest.mark.parametrize("patience", [1, 2, 3])
+def test_switch_linear_rise_closed_form(patience):
+    # d_t = 1 + t: every drop is negative (flat), so tau1 = patience; in the
+    # parallel stage the minimum stays 1 + tau1 and d_j > 1.1 (1 + tau1) holds
+    # for every j > tau1 once j > 0.1 (1 + tau1), i.e. for all j here, so
+    # tau2 = tau1 + patience.
+    d = [1.0 + t for t in range(20)]
+    tau1, tau2 = patience, 2 * patience
+    want = [0] * tau1 + [1] * (tau2 - tau1) + [2] * (20 - tau2)
+    assert oracle.switch_stages(d, 0.05, 0.10, patience) == want
+
+
+def test_switch_constant_series_parallel_forever():
+    assert oracle.switch_stages([0.3] * 12, 0.01, 0.01, 3) == [0] * 3 + [1] * 9
+
+
+def test_switch_is_scale_invariant_and_monotone():
+    rng = np.random.default_rng(77)
+    for trial in range(50):
+        t = np.arange(40)
+        d = list(0.2 + (t / 40.0 - 0.5) ** 2 + 0.01 * rng.standard_normal(40))
+        d = [abs(x) for x in d]
+        p = 1 + trial % 3
+        base = oracle.switch_stages(d, 0.03, 0.05, p)
+        assert all(a <= b for a, b in zip(base, base[1:]))
+        assert base[:p] == [0] * p
+        for c in (2.0 ** -10, 2.0 ** 13):  # exact scalings: the rules are relative
+            assert oracle.switch_stages([c * x for x in d], 0.03, 0.05, p) == base
+
+
+def test_switch_patience_ignores_a_single_spike():
+    d = [1.0, 0.5, 0.49, 0.485, 0.482, 0.60, 0.481, 0.480, 0.479]
+    assert oracle.switch_stages(d, 0.05, 0.10, 2) == [0, 0, 0, 1, 1, 1, 1, 1, 1]
+    assert oracle.switch_stages(d, 0.05, 0.10, 1) == [0, 0, 1, 1, 1, 2, 2, 2, 2]
+
+
+def test_switch_skips_nan_and_negative_entries():
+    bad = [float("nan"), -1.0]
+    for pos in range(len(SWITCH_SERIES) + 1):
+        d = SWITCH_SERIES[:pos] + bad + SWITCH_SERIES[pos:]
+        want = SWITCH_STAGES[:pos] + [SWITCH_STAGES[pos - 1] if pos else 0] * 2 + \
+            SWITCH_STAGES[pos:]
+        assert oracle.switch_stages(d, 0.05, 0.10, 2) == want
