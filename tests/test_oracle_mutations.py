@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
+import oracle.blocks as ob
 import oracle.displaced as od
 import tests.test_oracle_pins as pins
 
@@ -160,6 +161,32 @@ def _switch_variant(absolute_drop=False, rise_vs_previous=False, short_window=Fa
     return stages
 
 
+def _geglu_gate_first(X, W1, b1):
+    Hd = ob.linear(X, W1, b1)
+    n = Hd.shape[-1] // 2
+    return ob.gelu(Hd[..., :n]) * Hd[..., n:]
+
+
+def _resnet_no_silu_after_gn2(x, states, prm, P, G, eps):
+    st = states or {}
+    g1 = ob.silu(od.displaced_groupnorm(x, st.get("gn1", x), G, eps, prm["gn1_g"],
+                                        prm["gn1_b"], P))
+    h = od.displaced_conv3x3(g1, st.get("conv1", g1), prm["conv1_w"], prm["conv1_b"], P)
+    g2 = od.displaced_groupnorm(h, st.get("gn2", h), G, eps, prm["gn2_g"], prm["gn2_b"], P)
+    y = od.displaced_conv3x3(g2, st.get("conv2", g2), prm["conv2_w"], prm["conv2_b"], P)
+    return x + y, {"gn1": x, "conv1": g1, "gn2": h, "conv2": g2}
+
+
+def _resnet_states_swapped(x, states, prm, P, G, eps):
+    out, st = _orig_resnet(x, states, prm, P, G, eps)
+    st = dict(st)
+    st["conv1"], st["conv2"] = st["conv2"], st["conv1"]
+    return out, st
+
+
+_orig_resnet = ob.resnet_block
+
+
 MUTATIONS = {
     "conv_taps_transposed": [("_conv_row", _conv_row_transposed)],
     "conv_halo_fresh": [("displaced_conv3x3", _displaced_conv_fresh_halo)],
@@ -179,6 +206,9 @@ MUTATIONS = {
     "switch_absolute_drop": [("switch_stages", _switch_variant(absolute_drop=True))],
     "switch_rise_vs_previous": [("switch_stages", _switch_variant(rise_vs_previous=True))],
     "switch_short_window": [("switch_stages", _switch_variant(short_window=True))],
+    "geglu_gate_first": [("blocks.geglu", _geglu_gate_first)],
+    "resnet_no_silu_after_gn2": [("blocks.resnet_block", _resnet_no_silu_after_gn2)],
+    "resnet_states_swapped": [("blocks.resnet_block", _resnet_states_swapped)],
 }
 
 
@@ -203,6 +233,9 @@ def _all_pins():
 @pytest.mark.parametrize("mutation", sorted(MUTATIONS))
 def test_planted_mistake_fails_a_pin(mutation, monkeypatch):
     for attr, repl in MUTATIONS[mutation]:
+        if attr.startswith("blocks."):
+            monkeypatch.setattr(ob, attr.split(".", 1)[1], repl)
+            continue
         monkeypatch.setattr(od, attr, repl)
         if hasattr(oracle, attr):
             monkeypatch.setattr(oracle, attr, repl)

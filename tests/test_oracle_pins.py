@@ -567,3 +567,119 @@ def test_switch_skips_nan_and_negative_entries():
         want = SWITCH_STAGES[:pos] + [SWITCH_STAGES[pos - 1] if pos else 0] * 2 + \
             SWITCH_STAGES[pos:]
         assert oracle.switch_stages(d, 0.05, 0.10, 2) == want
+
+
+# ------------------------------------------------------------ block chain
+import oracle.blocks as OB  # noqa: E402
+
+
+def block_params(C, C_ctx, rng, ff_mult=4):
+    n = lambda *s: rng.standard_normal(s)
+    res = {"gn1_g": 1 + 0.1 * n(C), "gn1_b": 0.1 * n(C), "conv1_w": n(C, C, 3, 3) / np.sqrt(9 * C),
+           "conv1_b": 0.1 * n(C), "gn2_g": 1 + 0.1 * n(C), "gn2_b": 0.1 * n(C),
+           "conv2_w": n(C, C, 3, 3) / np.sqrt(9 * C), "conv2_b": 0.1 * n(C)}
+    F_ = ff_mult * C
+    tf = {"gn_g": 1 + 0.1 * n(C), "gn_b": 0.1 * n(C), "pi_w": n(C, C) / np.sqrt(C),
+          "pi_b": 0.1 * n(C), "po_w": n(C, C) / np.sqrt(C), "po_b": 0.1 * n(C),
+          "wq": n(C, C) / np.sqrt(C), "wk": n(C, C) / np.sqrt(C), "wv": n(C, C) / np.sqrt(C),
+          "wo": n(C, C) / np.sqrt(C), "xq": n(C, C) / np.sqrt(C),
+          "xk": n(C, C_ctx) / np.sqrt(C_ctx), "xv": n(C, C_ctx) / np.sqrt(C_ctx),
+          "xo": n(C, C) / np.sqrt(C), "ff1_w": n(2 * F_, C) / np.sqrt(C), "ff1_b": 0.1 * n(2 * F_),
+          "ff2_w": n(C, F_) / np.sqrt(F_), "ff2_b": 0.1 * n(C)}
+    for k in ("ln1", "ln2", "ln3"):
+        tf[k + "_g"], tf[k + "_b"] = 1 + 0.1 * n(C), 0.1 * n(C)
+    return res, tf
+
+
+def torch_resblock(x, prm, G, eps):
+    T = lambda k: t64(prm[k])
+    X = t64(x).permute(0, 3, 1, 2)
+    h = TF.conv2d(TF.silu(TF.group_norm(X, G, T("gn1_g"), T("gn1_b"), eps)), T("conv1_w"),
+                  T("conv1_b"), padding=1)
+    y = TF.conv2d(TF.silu(TF.group_norm(h, G, T("gn2_g"), T("gn2_b"), eps)), T("conv2_w"),
+                  T("conv2_b"), padding=1)
+    return (X + y).permute(0, 2, 3, 1).numpy()
+
+
+def torch_attention(q_in, kv_in, wq, wk, wv, wo, heads):
+    B, N, C = q_in.shape
+    d = C // heads
+    split = lambda t: t.reshape(B, t.shape[1], heads, d).transpose(1, 2)
+    o = TF.scaled_dot_product_attention(split(TF.linear(q_in, wq)), split(TF.linear(kv_in, wk)),
+                                        split(TF.linear(kv_in, wv)))
+    return TF.linear(o.transpose(1, 2).reshape(B, N, C), wo)
+
+
+def torch_transformer(x, ctx, prm, heads, G, eps_gn, eps_ln):
+    T = lambda k: t64(prm[k])
+    B, H, W, C = x.shape
+    X = t64(x)
+    g = TF.group_norm(X.permute(0, 3, 1, 2), G, T("gn_g"), T("gn_b"), eps_gn)
+    h = TF.linear(g.permute(0, 2, 3, 1).reshape(B, H * W, C), T("pi_w"), T("pi_b"))
+    t = TF.layer_norm(h, (C,), T("ln1_g"), T("ln1_b"), eps_ln)
+    h = h + torch_attention(t, t, T("wq"), T("wk"), T("wv"), T("wo"), heads)
+    t = TF.layer_norm(h, (C,), T("ln2_g"), T("ln2_b"), eps_ln)
+    h = h + torch_attention(t, t64(ctx), T("xq"), T("xk"), T("xv"), T("xo"), heads)
+    t = TF.layer_norm(h, (C,), T("ln3_g"), T("ln3_b"), eps_ln)
+    a, gate = TF.linear(t, T("ff1_w"), T("ff1_b")).chunk(2, dim=-1)
+    h = h + TF.linear(a * TF.gelu(gate), T("ff2_w"), T("ff2_b"))
+    return (X + TF.linear(h, T("po_w"), T("po_b")).reshape(B, H, W, C)).numpy()
+
+
+def test_layer_norm_gelu_silu_geglu_equal_torch():
+    X = rnd(3, 7, 24)
+    g, b = 1 + 0.1 * rnd(24), 0.1 * rnd(24)
+    want = TF.layer_norm(t64(X), (24,), t64(g), t64(b), 1e-5).numpy()
+    assert np.allclose(OB.layer_norm(X, 1e-5, g, b), want, rtol=0, atol=1e-12)
+    assert np.allclose(OB.gelu(X), TF.gelu(t64(X)).numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(OB.silu(X), TF.silu(t64(X)).numpy(), rtol=0, atol=1e-12)
+    W1, b1 = rnd(2 * 10, 24), rnd(2 * 10)
+    a, gate = TF.linear(t64(X), t64(W1), t64(b1)).chunk(2, dim=-1)
+    assert np.allclose(OB.geglu(X, W1, b1), (a * TF.gelu(gate)).numpy(), rtol=0, atol=1e-12)
+
+
+def test_gelu_closed_forms():
+    # GELU(0) = 0, GELU(x) - GELU(-x) = x, GELU(x) -> x for large x
+    x = np.linspace(-4, 4, 33)
+    assert OB.gelu(np.zeros(1))[0] == 0.0
+    assert np.allclose(OB.gelu(x) - OB.gelu(-x), x, atol=1e-14)
+    assert abs(OB.gelu(np.array([10.0]))[0] - 10.0) < 1e-12
+
+
+@pytest.mark.parametrize("P", [1, 2, 4])
+def test_resnet_block_synchronous_step_equals_torch(P):
+    rng = np.random.default_rng(31 + P)
+    x = rng.standard_normal((2, 8, 5, 16))
+    prm, _ = block_params(16, 12, rng)
+    out, st = OB.resnet_block(x, None, prm, P, 4, 1e-5)
+    assert np.allclose(out, torch_resblock(x, prm, 4, 1e-5), rtol=0, atol=1e-10)
+    assert set(st) == set(OB.RESNET_STATES)
+
+
+@pytest.mark.parametrize("P", [1, 2, 4])
+def test_transformer_block_synchronous_step_equals_torch(P):
+    rng = np.random.default_rng(41 + P)
+    x = rng.standard_normal((2, 8, 3, 16))
+    ctx = rng.standard_normal((2, 5, 12))
+    _, prm = block_params(16, 12, rng)
+    out, st = OB.transformer_block(x, ctx, None, prm, 2, P, 4, 1e-6, 1e-5)
+    assert np.allclose(out, torch_transformer(x, ctx, prm, 2, 4, 1e-6, 1e-5), rtol=0, atol=1e-10)
+    assert set(st) == set(OB.TRANSFORMER_STATES)
+
+
+def test_block_chain_states_route_to_their_layers():
+    # With the same input twice, every layer's input repeats, so the second,
+    # displaced step (fed the first step's states) equals the synchronous one;
+    # a state handed to the wrong layer breaks this.
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((1, 8, 4, 16))
+    ctx = rng.standard_normal((1, 5, 12))
+    pr, pt = block_params(16, 12, rng)
+    out0, st = OB.block_chain(x, ctx, None, pr, pt, 2, 4, 4, 1e-5, 1e-6, 1e-5)
+    out1, st1 = OB.block_chain(x, ctx, st, pr, pt, 2, 4, 4, 1e-5, 1e-6, 1e-5)
+    assert np.allclose(out1, out0, rtol=0, atol=1e-12)
+    # and with a changed input the displaced step differs from the synchronous one
+    x2 = x + 0.3 * rng.standard_normal(x.shape)
+    sync, _ = OB.block_chain(x2, ctx, None, pr, pt, 2, 4, 4, 1e-5, 1e-6, 1e-5)
+    disp, _ = OB.block_chain(x2, ctx, st, pr, pt, 2, 4, 4, 1e-5, 1e-6, 1e-5)
+    assert np.abs(disp - sync).max() > 1e-3
