@@ -3,8 +3,10 @@
 
 A step runs, through the C ABI, on the SDXL-3840px-with-guidance workload
 (latent 480x480, batch 2 = conditional + unconditional, 8 bands):
-  1. displaced 3x3 conv 320->320 on [2,480,480,320]        (dpp_conv3x3)
-  2. displaced GroupNorm (32 groups) on the conv output     (dpp_groupnorm)
+  1. displaced 3x3 conv 320->320 on [2,480,480,320], its
+     epilogue also summing the output per band and group  (dpp_conv3x3_gn)
+  2. displaced GroupNorm (32 groups) on the conv output,
+     one pass on those sums                                (dpp_groupnorm_apply)
   3. displaced self-attention, 2 x 57600 tokens, C=640,
      10 heads of 64: QKV projection writing the fresh K/V
      state, attention core, output projection             (dpp_self_attn)
@@ -21,7 +23,12 @@ projections + cross-attention; the bandwidth ops add time but no FLOPs),
 with per-op numbers and roofline fractions alongside.  Inputs and the step's
 working set (~2.5 GB) exceed the 126 MB L2, so no explicit flush is done.
 
+After the step, `block_chain` reports one level of the U-Net stepped the same
+way (ResNet block + transformer block at 2 x 240 x 240 x 640, 8 bands;
+14 ops per step through the same library), timed per displaced step.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--no-chain] [--no-cpu-baseline]
 """
 from __future__ import annotations
 
@@ -393,6 +400,62 @@ class OracleSample:
         return conv_f + self_f + cross_f, secs, desc
 
 
+def time_chain(dev, steps, warmup=2):
+    """One level of the U-Net (ResNet block + transformer block) stepped
+    with displaced patch parallelism at 3840px: latent 2 x 240 x 240 x 640 in
+    8 bands, 10 heads, text context 77 x 2048.  Times `steps` displaced steps
+    back to back, then the same number again with an event pair around every
+    op; returns the per-step figures."""
+    import displaced_patch_parallelism_02_b300 as dpp
+    from displaced_patch_parallelism_02_b300.chain import OPS, BlockChain
+    ch = wl.CHAINS["sdxl_3840_level2"]
+    wts = {}
+    for k, v in wl.chain_weights(ch).items():
+        if k.startswith("conv") and k.endswith("_w"):
+            v = v.permute(0, 2, 3, 1)  # channels-last [C, 3, 3, C]
+        wts[k] = v.contiguous().to(dev)
+    xs, ctx = wl.chain_inputs(ch, 0)
+    x, ctx = xs[0].to(dev), ctx.to(dev)
+    del xs
+    chain = BlockChain(ch.B, ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx, wts, dev,
+                       ff_mult=ch.ff_mult)
+    s = torch.cuda.current_stream(dev)
+    for _ in range(max(warmup, 1)):  # the first step is the synchronous one
+        chain.step(x, ctx, stream=s)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = dpp.dpp_launch_count()
+    a.record(s)
+    for _ in range(steps):
+        chain.step(x, ctx, stream=s)
+    b.record(s)
+    torch.cuda.synchronize(dev)
+    launches = (dpp.dpp_launch_count() - n0) // max(steps, 1)
+    ms = a.elapsed_time(b) / max(steps, 1)
+    evs = []
+
+    def hook(name, when, tensors):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(s)
+        evs.append((name, when, e))
+
+    for _ in range(steps):
+        chain.step(x, ctx, stream=s, hook=hook)
+    torch.cuda.synchronize(dev)
+    op_ms = {n: 0.0 for n in OPS}
+    for (n, w1, e1), (_, w2, e2) in zip(evs[0::2], evs[1::2]):
+        op_ms[n] += e1.elapsed_time(e2) / max(steps, 1)
+    ok = dpp.dpp_device_status() == dpp.DPP_OK and bool(torch.isfinite(x.float()).all())
+    flop = chain.flops()
+    del chain, wts, x, ctx
+    torch.cuda.empty_cache()
+    return {"workload": ch.name, "latent": [ch.B, ch.H, ch.W, ch.C], "P": ch.P,
+            "heads": ch.heads, "context": [ch.n_ctx, ch.c_ctx], "steps": steps,
+            "ms_per_step": ms, "tflops": flop / (ms / 1e3) / 1e12, "step_flop": flop,
+            "launches_per_step": launches, "ok": ok,
+            "ops_ms": {n: round(v, 4) for n, v in op_ms.items()}}
+
+
 def cpu_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -449,6 +512,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the ResNet + transformer block chain timing")
     ap.add_argument("--workload", default=WORKLOAD, choices=["sdxl_3840_cfg", "sdxl_2048"],
                     help="sdxl_2048 (no guidance maps or text context) is the smaller case "
                          "used for profiler captures")
@@ -604,6 +669,11 @@ def main():
             e2e_ms = float(t.item())
         e2e_val = model["step_flop"] * ws * K / (e2e_ms / 1e3) / 1e12
 
+    chain = None
+    if not args.no_chain and K > 0:
+        chain = time_chain(dev, K)
+        chain["frac_of_sustained_bf16"] = chain["tflops"] / sus
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         f, secs, desc = OracleSample(w).run()
@@ -635,6 +705,7 @@ def main():
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "switch_stages": stages},
             "gpu_launches": launches,
+            "block_chain": chain,
             "clocks": clocks,
         }
         print(json.dumps(line))

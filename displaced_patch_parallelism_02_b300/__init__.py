@@ -39,6 +39,12 @@ DPP_HALO_STALE = 0
 DPP_HALO_FRESH = 1
 DPP_HALO_ZERO = 2
 
+DPP_ACT_NONE = 0
+DPP_ACT_SILU = 1
+
+DPP_EPI_NONE = 0
+DPP_EPI_GEGLU = 1
+
 
 class DppError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -50,20 +56,32 @@ class DppError(RuntimeError):
 class dpp_conv_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
                 ("C_in", ctypes.c_int), ("C_out", ctypes.c_int), ("P", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("halo", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("halo", ctypes.c_int), ("accumulate", ctypes.c_int)]
 
 
 class dpp_gn_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
                 ("C", ctypes.c_int), ("G", ctypes.c_int), ("P", ctypes.c_int),
-                ("eps", ctypes.c_float), ("dtype", ctypes.c_int), ("band_local", ctypes.c_int)]
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int), ("band_local", ctypes.c_int),
+                ("act", ctypes.c_int)]
 
 
 class dpp_attn_desc(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
                 ("C", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("P", ctypes.c_int), ("n_ctx", ctypes.c_int), ("c_ctx", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("band_local", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("band_local", ctypes.c_int),
+                ("accumulate", ctypes.c_int)]
+
+
+class dpp_ln_desc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("C", ctypes.c_int), ("eps", ctypes.c_float),
+                ("dtype", ctypes.c_int)]
+
+
+class dpp_linear_desc(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int), ("K", ctypes.c_int), ("N", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("epilogue", ctypes.c_int), ("accumulate", ctypes.c_int)]
 
 
 class dpp_switch_state(ctypes.Structure):
@@ -105,6 +123,8 @@ _SIGNATURES = {
     "dpp_version": (ctypes.c_int, []),
     "dpp_launch_count": (ctypes.c_uint64, []),
     "dpp_set_attn_core_events": (None, [_vp, _vp]),
+    "dpp_layernorm": (_st, [ctypes.POINTER(dpp_ln_desc), _vp, _vp, _vp, _vp, _vp]),
+    "dpp_linear": (_st, [ctypes.POINTER(dpp_linear_desc), _vp, _vp, _vp, _vp, _vp]),
     "dpp_switch_init": (None, [ctypes.POINTER(dpp_switch_state), ctypes.c_double,
                                ctypes.c_double, ctypes.c_int]),
     "dpp_switch_update": (ctypes.c_int, [ctypes.POINTER(dpp_switch_state), ctypes.c_double]),
@@ -195,6 +215,20 @@ def dpp_groupnorm_apply(desc: dpp_gn_desc, x, stats_prev, gn_sums, stats_next, g
                                           _ptr(gn_sums), _ptr(stats_next), _ptr(gamma),
                                           _ptr(beta), _ptr(y), _stream(stream)),
                   "dpp_groupnorm_apply", raise_on_error)
+
+
+def dpp_layernorm(desc: dpp_ln_desc, x, gamma, beta, y, stream=None,
+                  raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_layernorm(ctypes.byref(desc), _ptr(x), _ptr(gamma), _ptr(beta),
+                                    _ptr(y), _stream(stream)),
+                  "dpp_layernorm", raise_on_error)
+
+
+def dpp_linear(desc: dpp_linear_desc, x, w, bias, y, stream=None,
+               raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_linear(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
+                                 _stream(stream)),
+                  "dpp_linear", raise_on_error)
 
 
 def dpp_groupnorm_workspace_bytes(desc: dpp_gn_desc) -> int:

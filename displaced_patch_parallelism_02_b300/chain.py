@@ -1,0 +1,175 @@
+"""SDXL-shaped block chain stepped with displaced patch parallelism.
+
+One level of the U-Net's down path: a ResNet block followed by a transformer
+block, on an NHWC latent of B x H x W x C cut into P bands of rows.  Every
+layer is a call into libdpp (this module only sequences the calls and owns the
+buffers); the layers DistriFusion replaces (convolutions, GroupNorms, self-
+attention) read the previous step's state of the other bands, the per-token
+layers (LayerNorm, projections, the gated feed-forward) need none:
+
+  ResNet block   g1 = SiLU(GN1(x))              dpp_groupnorm (act SiLU)
+                 h1 = conv1(g1) + b1            dpp_conv3x3_gn (sums for GN2)
+                 g2 = SiLU(GN2(h1))             dpp_groupnorm_apply (act SiLU)
+                 x += conv2(g2) + b2            dpp_conv3x3_gn (accumulate; sums for GN)
+  transformer    g = GN(x)                      dpp_groupnorm_apply
+                 h = g Wpi^T + bpi              dpp_linear
+                 h += attn1(LN1(h))             dpp_layernorm, dpp_self_attn (accumulate)
+                 h += attn2(LN2(h), ctx)        dpp_layernorm, dpp_cross_attn (accumulate)
+                 h += GEGLU(LN3(h)) W2^T + b2   dpp_layernorm, dpp_linear (GEGLU), dpp_linear
+                 x += h Wpo^T + bpo             dpp_linear (accumulate)
+
+The chain runs in place on x (the residual stream).  On one GPU every band's
+fresh activations of step t are all in HBM, so the stale state of step t+1 is
+simply step t's fresh buffer: the conv inputs, GroupNorm partials and K/V
+state are double-buffered and swapped each step (the refresh costs nothing).
+The time embedding is the same for both images of a guidance pair, so it is
+part of conv1's bias.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (DPP_ACT_SILU, DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_attn_desc,
+               dpp_conv3x3_gn, dpp_conv_desc, dpp_cross_attn, dpp_cross_attn_workspace_bytes,
+               dpp_gn_desc, dpp_groupnorm, dpp_groupnorm_apply, dpp_groupnorm_workspace_bytes,
+               dpp_layernorm, dpp_linear, dpp_linear_desc, dpp_ln_desc, dpp_self_attn,
+               dpp_self_attn_workspace_bytes)
+
+# weight names (torch layouts: conv [C, C, 3, 3] is passed channels-last,
+# i.e. [C, 3, 3, C]; Linear [out, in]; biases and affines fp32)
+RESNET_WEIGHTS = ("gn1_g", "gn1_b", "conv1_w", "conv1_b", "gn2_g", "gn2_b", "conv2_w", "conv2_b")
+TRANSFORMER_WEIGHTS = ("gn_g", "gn_b", "pi_w", "pi_b", "ln1_g", "ln1_b", "wq", "wk", "wv", "wo",
+                       "ln2_g", "ln2_b", "xq", "xk", "xv", "xo", "ln3_g", "ln3_b", "ff1_w",
+                       "ff1_b", "ff2_w", "ff2_b", "po_w", "po_b")
+OPS = ("gn1", "conv1", "gn2", "conv2", "gn", "proj_in", "ln1", "attn1", "ln2", "attn2", "ln3",
+       "ff1", "ff2", "proj_out")
+
+
+class BlockChain:
+    """Buffers, states and the call sequence of one displaced step of the
+    chain.  ``weights`` maps the names in RESNET_WEIGHTS and
+    TRANSFORMER_WEIGHTS to device tensors (bf16 weights, fp32 biases and
+    affines); ff1_w is [2 F, C] (value rows, then gate rows), ff2_w [C, F]."""
+
+    def __init__(self, B, H, W, C, heads, P, G, n_ctx, c_ctx, weights, device,
+                 ff_mult=4, eps_gn_res=1e-5, eps_gn_tf=1e-6, eps_ln=1e-5):
+        self.B, self.H, self.W, self.C, self.P, self.G = B, H, W, C, P, G
+        self.heads, self.n_ctx, self.c_ctx, self.F = heads, n_ctx, c_ctx, ff_mult * C
+        self.w = weights
+        dev = torch.device(device)
+        bf = torch.bfloat16
+        N, M = H * W, B * H * W
+        self.M = M
+        act = lambda *s: torch.empty(s, dtype=bf, device=dev)
+        img = (B, H, W, C)
+        self.g1 = [act(*img), act(*img)]   # conv1 input: fresh / previous step's
+        self.g2 = [act(*img), act(*img)]   # conv2 input
+        self.h1 = act(*img)
+        self.gt = act(B, N, C)             # transformer GroupNorm output
+        self.h = act(B, N, C)              # transformer residual stream
+        self.t = act(B, N, C)              # LayerNorm output
+        self.u = act(M, self.F)            # gated feed-forward hidden
+        stats = lambda: [torch.empty((P, B, G, 2), dtype=torch.float32, device=dev)
+                         for _ in range(2)]
+        self.st1, self.st2, self.stt = stats(), stats(), stats()
+        self.sums = [torch.empty((P, B, G, 2), dtype=torch.float64, device=dev)
+                     for _ in range(2)]
+        self.kv = [torch.empty((B, N, 2, C), dtype=torch.float16, device=dev) for _ in range(2)]
+        self.gn1 = dpp_gn_desc(B, H, W, C, G, P, eps_gn_res, DPP_BF16, 0, DPP_ACT_SILU)
+        self.gn2 = dpp_gn_desc(B, H, W, C, G, P, eps_gn_res, DPP_BF16, 0, DPP_ACT_SILU)
+        self.gnt = dpp_gn_desc(B, H, W, C, G, P, eps_gn_tf, DPP_BF16, 0, 0)
+        self.conv1 = dpp_conv_desc(B, H, W, C, C, P, DPP_BF16, 0, 0)
+        self.conv2 = dpp_conv_desc(B, H, W, C, C, P, DPP_BF16, 0, 1)
+        self.ln = dpp_ln_desc(M, C, eps_ln, DPP_BF16)
+        self.lin = dpp_linear_desc(M, C, C, DPP_BF16, DPP_EPI_NONE, 0)
+        self.lin_acc = dpp_linear_desc(M, C, C, DPP_BF16, DPP_EPI_NONE, 1)
+        self.ff1 = dpp_linear_desc(M, C, self.F, DPP_BF16, DPP_EPI_GEGLU, 0)
+        self.ff2 = dpp_linear_desc(M, self.F, C, DPP_BF16, DPP_EPI_NONE, 1)
+        self.sa = dpp_attn_desc(B, H, W, C, heads, C // heads, P, 0, 0, DPP_BF16, 0, 1)
+        self.xa = dpp_attn_desc(B, H, W, C, heads, C // heads, 1, n_ctx, c_ctx, DPP_BF16, 0, 1)
+        ws = lambda n: torch.empty(max(int(n), 16), dtype=torch.uint8, device=dev)
+        self.gn_ws_n = dpp_groupnorm_workspace_bytes(self.gn1)
+        self.sa_ws_n = dpp_self_attn_workspace_bytes(self.sa)
+        self.xa_ws_n = dpp_cross_attn_workspace_bytes(self.xa)
+        self.gn_ws, self.sa_ws, self.xa_ws = ws(self.gn_ws_n), ws(self.sa_ws_n), ws(self.xa_ws_n)
+        self.k = 0  # steps taken; step 0 is the synchronous one
+
+    def flops(self):
+        """Tensor FLOPs of one step (convolutions, projections, attention
+        cores, feed-forward); the normalisations are not counted."""
+        M, C, F, n = self.M, self.C, self.F, self.n_ctx
+        conv = 2 * (2.0 * M * C * 9 * C)
+        lin = 2 * (2.0 * M * C * C) + 2.0 * M * C * 2 * F + 2.0 * M * F * C
+        self_attn = 2.0 * M * C * 3 * C + 4.0 * M * self.H * self.W * C + 2.0 * M * C * C
+        cross = (2.0 * M * C * C + 2.0 * self.B * n * self.c_ctx * 2 * C + 4.0 * M * n * C
+                 + 2.0 * M * C * C)
+        return conv + lin + self_attn + cross
+
+    def step(self, x, ctx, stream=None, hook=None):
+        """One displaced step on x ([B, H, W, C] bf16, updated in place) with
+        the text context ctx ([B, n_ctx, c_ctx] bf16).  hook(op, when, tensors),
+        when given, is called before ("pre") and after ("post") every op with
+        the op's input and output tensors (for tests that check op by op)."""
+        w, s = self.w, stream
+        i, j = self.k % 2, 1 - self.k % 2
+        first = self.k == 0
+        prev = (lambda a: None) if first else (lambda a: a[j])
+        B, N, C = self.B, self.H * self.W, self.C
+        tok = x.view(B, N, C)
+        call = hook or (lambda *a: None)
+
+        def op(name, fn, ins, out):
+            call(name, "pre", dict(ins, out=out))
+            fn()
+            call(name, "post", dict(ins, out=out))
+
+        # ---------------------------------------------------------- ResNet block
+        op("gn1", lambda: dpp_groupnorm(self.gn1, x, prev(self.st1), self.st1[i], w["gn1_g"],
+                                        w["gn1_b"], self.g1[i], self.gn_ws, self.gn_ws_n,
+                                        stream=s),
+           {"x": x}, self.g1[i])
+        op("conv1", lambda: dpp_conv3x3_gn(self.conv1, self.g1[i], prev(self.g1), w["conv1_w"],
+                                           w["conv1_b"], self.h1, self.G, self.sums[0],
+                                           stream=s),
+           {"x": self.g1[i]}, self.h1)
+        op("gn2", lambda: dpp_groupnorm_apply(self.gn2, self.h1, prev(self.st2), self.sums[0],
+                                              self.st2[i], w["gn2_g"], w["gn2_b"], self.g2[i],
+                                              stream=s),
+           {"x": self.h1}, self.g2[i])
+        op("conv2", lambda: dpp_conv3x3_gn(self.conv2, self.g2[i], prev(self.g2), w["conv2_w"],
+                                           w["conv2_b"], x, self.G, self.sums[1], stream=s),
+           {"x": self.g2[i]}, x)
+        # ------------------------------------------------------ transformer block
+        op("gn", lambda: dpp_groupnorm_apply(self.gnt, x, prev(self.stt), self.sums[1],
+                                             self.stt[i], w["gn_g"], w["gn_b"], self.gt,
+                                             stream=s),
+           {"x": x}, self.gt)
+        op("proj_in", lambda: dpp_linear(self.lin, self.gt, w["pi_w"], w["pi_b"], self.h,
+                                         stream=s),
+           {"x": self.gt}, self.h)
+        op("ln1", lambda: dpp_layernorm(self.ln, self.h, w["ln1_g"], w["ln1_b"], self.t,
+                                        stream=s),
+           {"x": self.h}, self.t)
+        op("attn1", lambda: dpp_self_attn(self.sa, self.t, w["wq"], w["wk"], w["wv"], w["wo"],
+                                          prev(self.kv), self.kv[i], self.h, self.sa_ws,
+                                          self.sa_ws_n, stream=s),
+           {"x": self.t}, self.h)
+        op("ln2", lambda: dpp_layernorm(self.ln, self.h, w["ln2_g"], w["ln2_b"], self.t,
+                                        stream=s),
+           {"x": self.h}, self.t)
+        op("attn2", lambda: dpp_cross_attn(self.xa, self.t, ctx, w["xq"], w["xk"], w["xv"],
+                                           w["xo"], self.h, self.xa_ws, self.xa_ws_n, stream=s),
+           {"x": self.t, "ctx": ctx}, self.h)
+        op("ln3", lambda: dpp_layernorm(self.ln, self.h, w["ln3_g"], w["ln3_b"], self.t,
+                                        stream=s),
+           {"x": self.h}, self.t)
+        op("ff1", lambda: dpp_linear(self.ff1, self.t, w["ff1_w"], w["ff1_b"], self.u,
+                                     stream=s),
+           {"x": self.t}, self.u)
+        op("ff2", lambda: dpp_linear(self.ff2, self.u, w["ff2_w"], w["ff2_b"], self.h,
+                                     stream=s),
+           {"x": self.u}, self.h)
+        op("proj_out", lambda: dpp_linear(self.lin_acc, self.h, w["po_w"], w["po_b"], tok,
+                                          stream=s),
+           {"x": self.h}, tok)
+        self.k += 1

@@ -142,6 +142,7 @@ cudaError_t out_proj(const dpp_attn_desc &d, const void *o, const void *wo, void
     tw = E_F16;
   }
   GemmArgs op{o, {w, nullptr, nullptr}, C, M, C, C, y, C, C, nullptr, 0, te, tw, tl};
+  op.accumulate = d.accumulate ? 1 : 0;  // y += O wo^T: the block's residual addition
   return gemm(op, s);
 }
 
@@ -432,6 +433,56 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
   const size_t nkvb = (size_t)d->B * d->n_ctx * 2 * d->C * elem_bytes(te);
   return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256) + align_up(nkvb, 256), y,
                             (int)nt, s));
+}
+
+// ---------------------------------------------------- per-token layers
+dpp_status dpp_layernorm(const dpp_ln_desc *d, const void *x, const float *gamma,
+                         const float *beta, void *y, dpp_stream stream) {
+  if (!d || !x || !y || !dtype_ok(d->dtype)) return DPP_ERR_INVALID_ARG;
+  if (d->T < 1 || d->C < 1 || !(d->eps >= 0.f)) return DPP_ERR_INVALID_ARG;
+  if ((gamma == nullptr) != (beta == nullptr)) return DPP_ERR_INVALID_ARG;
+  const int q = chan_quantum(d->dtype);
+  if (d->C % q) return DPP_ERR_INVALID_ARG;
+  if (d->C > 256 * q) return DPP_ERR_UNSUPPORTED;
+  if ((long long)d->T * d->C > kMaxElems) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y) || (gamma && !aligned16(gamma)) ||
+      (beta && !aligned16(beta)))
+    return DPP_ERR_ALIGN;
+  const size_t n = (size_t)d->T * d->C * elem_size(d->dtype);
+  if (y != x && overlap(y, n, x, n)) return DPP_ERR_ALIAS;
+  if (overlap(y, n, gamma, d->C * sizeof(float)) || overlap(y, n, beta, d->C * sizeof(float)))
+    return DPP_ERR_ALIAS;
+  return from_cuda(
+      counted(launch_layernorm(*d, x, gamma, beta, y, (cudaStream_t)stream), 1));
+}
+
+dpp_status dpp_linear(const dpp_linear_desc *d, const void *x, const void *w, const float *bias,
+                      void *y, dpp_stream stream) {
+  if (!d || !x || !w || !y || !dtype_ok(d->dtype)) return DPP_ERR_INVALID_ARG;
+  if (d->M < 1 || d->K < 1 || d->N < 1) return DPP_ERR_INVALID_ARG;
+  if (d->epilogue != DPP_EPI_NONE && d->epilogue != DPP_EPI_GEGLU) return DPP_ERR_INVALID_ARG;
+  if (d->dtype != DPP_BF16) return DPP_ERR_UNSUPPORTED;
+  if (d->K % 8 || d->N % 64) return DPP_ERR_INVALID_ARG;
+  const bool geglu = d->epilogue == DPP_EPI_GEGLU;
+  const long long wrows = geglu ? 2ll * d->N : d->N;
+  if ((long long)d->M * d->K > kMaxElems || (long long)d->M * d->N > kMaxElems ||
+      wrows * d->K > kMaxElems)
+    return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)))
+    return DPP_ERR_ALIGN;
+  const size_t nx = (size_t)d->M * d->K * 2, ny = (size_t)d->M * d->N * 2;
+  const size_t nw = (size_t)wrows * d->K * 2;
+  if (overlap(y, ny, x, nx) || overlap(y, ny, w, nw) ||
+      overlap(y, ny, bias, (size_t)wrows * sizeof(float)))
+    return DPP_ERR_ALIAS;
+  const char *wb = reinterpret_cast<const char *>(w);
+  GemmArgs g{x, {w, geglu ? wb + (size_t)d->N * d->K * 2 : nullptr, nullptr}, d->N, d->M, d->N,
+             d->K, y, d->N, d->N, nullptr, 0, E_BF16, E_BF16, E_BF16};
+  g.bias = bias;
+  g.accumulate = d->accumulate ? 1 : 0;
+  g.geglu = geglu ? 1 : 0;
+  if (!gemm_tc_supported(g)) return DPP_ERR_UNSUPPORTED;
+  return from_cuda(counted(launch_gemm_tc(g, device_status_ptr(), (cudaStream_t)stream), 1));
 }
 
 }  // extern "C"

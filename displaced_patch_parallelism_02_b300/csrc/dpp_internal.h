@@ -91,6 +91,10 @@ struct GemmArgs {
   void *out1;
   int ld1;
   Elem ta, tb, to;
+  const float *bias = nullptr;  // [N] fp32 added to out0's columns ([2 Nout] with geglu)
+  int accumulate = 0;           // out0 += result (out0 read first)
+  int geglu = 0;                // B[0] = value rows, B[1] = gate rows (b_rows = N each):
+                                // out0 = value * GELU(gate), N output columns
 };
 cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s);
@@ -115,6 +119,10 @@ struct AttnArgs {
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s);
 bool attn_tc_supported(const AttnArgs &a);
+
+// token-wise LayerNorm (C <= 256 16-byte vectors)
+cudaError_t launch_layernorm(const dpp_ln_desc &d, const void *x, const float *gamma,
+                             const float *beta, void *y, cudaStream_t s);
 
 // device status word (bounded waits record DPP_ERR_TIMEOUT here)
 int *device_status_ptr();

@@ -17,7 +17,8 @@
 //               [C_out][3][3][C_in], 128-byte swizzle, STAGES-deep ring;
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer
 //               (M 128, N BN, K 16), two accumulators 256 columns apart;
-//   warps 2..5  epilogue: tcgen05.ld, + bias, bf16, 16-byte stores; with
+//   warps 2..5  epilogue: tcgen05.ld, + bias (+ the residual already in y
+//               when accumulating), bf16, 16-byte stores; with
 //               STATS also the per-group sums of the stored values (for a
 //               GroupNorm of this output), reduced over the warp's 32 pixels
 //               and added into fp64 totals per (band, image, group).
@@ -35,6 +36,7 @@ struct ConvTcParams {
   int m_tiles, n_tiles;
   int use_stale; // 0: every input row comes from the fresh map
   int zero_halo; // 1: rows outside the band read as zero (naive patches)
+  int accumulate; // 1: y += result (the residual already in y is read first)
   const float *bias;
   __nv_bfloat16 *y;
   int *status;
@@ -216,6 +218,12 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int n = n0 + c * 32;
         float st1[32], st2[32];  // STATS: this pixel's stored values and their squares
         if (w < p.W && n < p.Cout) {
+          uint4 res[4];  // accumulate: the residual already in y, all four loads in flight
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            res[v] = p.accumulate && n + 8 * v < p.Cout
+                         ? *reinterpret_cast<const uint4 *>(yrow + n + 8 * v)
+                         : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int nv = n + 8 * v;
@@ -223,6 +231,14 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
               float bv[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) bv[e] = p.bias ? __ldg(p.bias + nv + e) : 0.f;
+              {  // bf16 -> fp32 is a 16-bit shift; zero when not accumulating
+                const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  bv[2 * e] += __uint_as_float(rw[e] << 16);
+                  bv[2 * e + 1] += __uint_as_float(rw[e] & 0xffff0000u);
+                }
+              }
               uint4 o;
               uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
@@ -327,6 +343,7 @@ cudaError_t run(const dpp_conv_desc &d, const CUtensorMap &mx, const CUtensorMap
   p.n_tiles = (d.C_out + BN - 1) / BN;
   p.use_stale = use_stale;
   p.zero_halo = zero_halo;
+  p.accumulate = d.accumulate ? 1 : 0;
   p.bias = bias;
   p.y = reinterpret_cast<__nv_bfloat16 *>(y);
   p.status = status;

@@ -62,6 +62,9 @@ struct GemmTcParams {
   int out_f16;  // 1: fp16 output, 0: bf16 output
   int m_tiles, n_tiles;
   int *status;
+  const float *bias;  // per out0 column ([2 N] with geglu: value then gate), or null
+  int accumulate;     // out0 += result
+  int geglu;          // tile = BN/2 value rows of B0 + BN/2 gate rows of B1
 };
 
 constexpr int kThreads = 192;
@@ -136,6 +139,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j) {
+            if (p.geglu) {  // value rows, then the matching gate rows
+              const bool gate = j >= BN / 128;
+              const int n = n0 / 2 + 64 * (gate ? j - BN / 128 : j);
+              tma_load_2d(sa + A_BYTES + j * 64 * 128, gate ? &tmB1 : &tmB0, &full[stage],
+                          kb * BK, n);
+              continue;
+            }
             const int n = n0 + 64 * j;
             int mat = n / p.b_rows;
             if (mat > 2) mat = 2;
@@ -202,6 +212,53 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_fence_after();
       const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
       const int m = m0 + row;
+      if (p.geglu) {
+        // value columns [0, BN/2) and gate columns [BN/2, BN) of the tile:
+        // out[n0/2 + j] = (value_j + b_j) * GELU(gate_j + b_{N + j})
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t rv[32], rg[32];
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32;
+          tmem_ld32(ta, rv);
+          tmem_ld32(ta + BN / 2, rg);
+          tmem_wait_ld();
+          const int n = n0 / 2 + c * 32;
+          if (m < p.M && n < p.N) {
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out0) + (size_t)m * p.ld0 + n;
+            uint4 res[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              res[v] = p.accumulate ? reinterpret_cast<const uint4 *>(dst)[v]
+                                    : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
+              uint4 o;
+              uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float f[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int k = v * 8 + 2 * e + h, col = n + k;
+                  const float a = __uint_as_float(rv[k]) + (p.bias ? __ldg(p.bias + col) : 0.f);
+                  const float g =
+                      __uint_as_float(rg[k]) + (p.bias ? __ldg(p.bias + p.N + col) : 0.f);
+                  f[h] = a * (0.5f * g * (1.f + erff(g * 0.70710678118654752f)));
+                }
+                f[0] += __uint_as_float(rw[e] << 16);
+                f[1] += __uint_as_float(rw[e] & 0xffff0000u);
+                ow[e] = pack_bf162(f[0], f[1]);
+              }
+              reinterpret_cast<uint4 *>(dst)[v] = o;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -210,20 +267,41 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int n = n0 + c * 32;
         if (m < p.M && n < p.N) {
           uint4 *dst;
-          if (n < p.split)
+          const bool first = n < p.split;
+          if (first)
             dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out0) +
                                             (size_t)m * p.ld0 + n);
           else
             dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out1) +
                                             (size_t)m * p.ld1 + (n - p.split));
+          const bool acc_in = first && p.accumulate;
+          uint4 res[4];  // the residual already in out0, all four loads in flight
+#pragma unroll
+          for (int v = 0; v < 4; ++v) res[v] = acc_in ? dst[v] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 o;
             uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+            const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float a = __uint_as_float(r[v * 8 + 2 * e]);
-              const float b = __uint_as_float(r[v * 8 + 2 * e + 1]);
+              const int col = n + v * 8 + 2 * e;
+              float a = __uint_as_float(r[v * 8 + 2 * e]);
+              float b = __uint_as_float(r[v * 8 + 2 * e + 1]);
+              if (first && p.bias) {
+                a += __ldg(p.bias + col);
+                b += __ldg(p.bias + col + 1);
+              }
+              if (acc_in) {  // out0 is bf16 or fp16, as the output
+                if (p.out_f16) {
+                  const float2 old = __half22float2(*reinterpret_cast<const __half2 *>(&rw[e]));
+                  a += old.x;
+                  b += old.y;
+                } else {
+                  a += __uint_as_float(rw[e] << 16);
+                  b += __uint_as_float(rw[e] & 0xffff0000u);
+                }
+              }
               ow[e] = p.out_f16 ? pack_half2(a, b) : pack_bf162(a, b);
             }
             dst[v] = o;
@@ -263,8 +341,10 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
     if (!encode_tiled(&mb[i], ty, 2, b, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  const int n_cols = g.geglu ? 2 * g.N : g.N;  // accumulator columns in all
   GemmTcParams p{g.M, g.N, g.K, g.b_rows, g.out0, g.ld0, g.split, g.out1, g.ld1,
-                 g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, (g.N + BN - 1) / BN, status};
+                 g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, (n_cols + BN - 1) / BN, status,
+                 g.bias, g.accumulate ? 1 : 0, g.geglu ? 1 : 0};
   constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512;
   auto k = gemm_tc_kernel<BN, STAGES, IN_BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -299,6 +379,9 @@ cudaError_t launch_cast_bf16_f16(const void *in, void *out, size_t n, cudaStream
 bool gemm_tc_supported(const GemmArgs &g) {
   const bool in16 = (g.ta == E_BF16 || g.ta == E_F16) && g.ta == g.tb;
   const bool out16 = g.to == E_BF16 || g.to == E_F16;
+  if (g.geglu)  // value / gate blocks of N rows; bf16 output; tiles of 64 or 128 columns
+    return in16 && g.to == E_BF16 && g.K % 8 == 0 && g.N % 64 == 0 && g.b_rows == g.N &&
+           g.split == g.N && g.out1 == nullptr && g.ld0 % 8 == 0 && g.M > 0 && g.B[1];
   return in16 && out16 && g.K % 8 == 0 && g.b_rows % 64 == 0 && g.N % 32 == 0 &&
          g.split % 32 == 0 && g.ld0 % 8 == 0 && (g.out1 == nullptr || g.ld1 % 8 == 0) &&
          (g.N + g.b_rows - 1) / g.b_rows <= 3 && g.M > 0;
@@ -307,6 +390,11 @@ bool gemm_tc_supported(const GemmArgs &g) {
 cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
   const bool bf = g.ta == E_BF16;
+  if (g.geglu) {  // a tile holds BN/2 value and BN/2 gate columns
+    if (g.N % 128 == 0)
+      return bf ? run<256, 4, true>(g, status, s) : run<256, 4, false>(g, status, s);
+    return bf ? run<128, 6, true>(g, status, s) : run<128, 6, false>(g, status, s);
+  }
   if (g.N % 192 == 0)
     return bf ? run<192, 5, true>(g, status, s) : run<192, 5, false>(g, status, s);
   if (g.N % 256 == 0)

@@ -117,6 +117,12 @@ __device__ __forceinline__ bool gn_bar_wait(uint64_t *bar, uint32_t parity, int 
   }
 }
 
+// The activation that may follow the affine (DPP_ACT_SILU: x * sigmoid(x),
+// the GroupNorm -> SiLU of a ResNet block).
+__device__ __forceinline__ float gn_act(float x, int act) {
+  return act == DPP_ACT_SILU ? x / (1.f + __expf(-x)) : x;
+}
+
 template <typename T>
 struct Vec16;
 
@@ -183,6 +189,7 @@ struct GnGeom {
   int R;      // pixel rows in flight per CTA (threads = R * C / VE)
   int sync;   // 1: no stale statistics
   int band_local;  // 1: each band's statistics over its own rows only
+  int act;    // DPP_ACT_* applied after the affine
   int ppp;    // pixels per prefetched piece (the shared-memory buffer)
 };
 
@@ -409,7 +416,7 @@ gn_fused_kernel(const T *x, T *y, GnGeom g, const float *__restrict__ stats_prev
             float f[VE];
             Vec16<T>::cvt(raw[k], f);
 #pragma unroll
-            for (int e = 0; e < VE; ++e) f[e] = fmaf(f[e], sc[e], sh[e]);
+            for (int e = 0; e < VE; ++e) f[e] = gn_act(fmaf(f[e], sc[e], sh[e]), g.act);
             gn_st_hint(y + (base + j + k * R) * g.C + v * VE, Vec16<T>::pack(f), drop);
           }
         }
@@ -537,6 +544,7 @@ cudaError_t run_gn(const dpp_gn_desc &d, const void *x, const float *stats_prev,
   g.R = R;
   g.sync = stats_prev == nullptr ? 1 : 0;
   g.band_local = d.band_local ? 1 : 0;
+  g.act = d.act;
   long long grid = (long long)per_sm * sms;
   if (grid > kGnMaxGrid) grid = kGnMaxGrid;
   // CTA groups work on different units at the same time, so one group's
@@ -594,7 +602,7 @@ namespace {
 template <typename T>
 __global__ void __launch_bounds__(512)
 gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int ppc, int band_local,
-                const double *__restrict__ gn_sums, const float *__restrict__ stats_prev,
+                int act, const double *__restrict__ gn_sums, const float *__restrict__ stats_prev,
                 float *__restrict__ stats_next, const float *__restrict__ gamma,
                 const float *__restrict__ beta, float eps) {
   constexpr int VE = Vec16<T>::N;
@@ -657,7 +665,7 @@ gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int 
         float f[VE];
         Vec16<T>::cvt(raw[k], f);
 #pragma unroll
-        for (int e = 0; e < VE; ++e) f[e] = fmaf(f[e], sc[e], sh[e]);
+        for (int e = 0; e < VE; ++e) f[e] = gn_act(fmaf(f[e], sc[e], sh[e]), act);
         gn_st_hint(y + (base + j + k * R) * C + v * VE, Vec16<T>::pack(f), drop);
       }
     }
@@ -683,11 +691,11 @@ cudaError_t launch_groupnorm_apply(const dpp_gn_desc &d, const void *x, const fl
   if (d.dtype == DPP_BF16)
     gn_apply_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
         (const __nv_bfloat16 *)x, (__nv_bfloat16 *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc,
-        d.band_local ? 1 : 0, gn_sums, stats_prev, stats_next, gamma, beta, d.eps);
+        d.band_local ? 1 : 0, d.act, gn_sums, stats_prev, stats_next, gamma, beta, d.eps);
   else
     gn_apply_kernel<float><<<grid, threads, 0, s>>>(
         (const float *)x, (float *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc, d.band_local ? 1 : 0,
-        gn_sums, stats_prev,
+        d.act, gn_sums, stats_prev,
         stats_next, gamma, beta, d.eps);
   return cudaGetLastError();
 }

@@ -44,6 +44,10 @@ __device__ __forceinline__ void load4<__half>(const __half *p, float f[4]) {
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+
 template <typename T>
 __device__ __forceinline__ T from_f(float v);
 template <>
@@ -59,7 +63,7 @@ constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
 
 // ----------------------------------------------------------------- conv
 struct ConvGeom {
-  int B, H, W, Ci, Co, P, fresh_halo, zero_halo;
+  int B, H, W, Ci, Co, P, fresh_halo, zero_halo, accumulate;
 };
 
 template <typename T>
@@ -122,7 +126,11 @@ conv_simt_kernel(const T *__restrict__ x, const T *__restrict__ stale, const T *
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int co = n0 + tx + 16 * j;
-      if (co < g.Co) y[(size_t)mm * g.Co + co] = from_f<T>(acc[i][j] + (bias ? bias[co] : 0.f));
+      if (co < g.Co) {
+        float v = acc[i][j] + (bias ? bias[co] : 0.f);
+        if (g.accumulate) v += to_f(y[(size_t)mm * g.Co + co]);
+        y[(size_t)mm * g.Co + co] = from_f<T>(v);
+      }
     }
   }
 }
@@ -176,9 +184,11 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const __grid_constant__ G
     for (int j = 0; j < 4; ++j) {
       const int nn = n0 + tx + 16 * j;
       if (nn >= g.N) continue;
-      if (nn < g.split)
-        o0[(size_t)mm * g.ld0 + nn] = from_f<TO>(acc[i][j]);
-      else
+      if (nn < g.split) {
+        float v = acc[i][j] + (g.bias ? g.bias[nn] : 0.f);
+        if (g.accumulate) v += to_f(o0[(size_t)mm * g.ld0 + nn]);
+        o0[(size_t)mm * g.ld0 + nn] = from_f<TO>(v);
+      } else
         o1[(size_t)mm * g.ld1 + (nn - g.split)] = from_f<TO>(acc[i][j]);
     }
   }
@@ -326,7 +336,7 @@ cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *
                              const void *w, const float *bias, void *y, cudaStream_t s) {
   const int fresh_halo = (d.halo == DPP_HALO_FRESH || stale == nullptr || stale == x) ? 1 : 0;
   const int zero_halo = d.halo == DPP_HALO_ZERO ? 1 : 0;
-  ConvGeom g{d.B, d.H, d.W, d.C_in, d.C_out, d.P, fresh_halo, zero_halo};
+  ConvGeom g{d.B, d.H, d.W, d.C_in, d.C_out, d.P, fresh_halo, zero_halo, d.accumulate ? 1 : 0};
   const void *st = fresh_halo ? x : stale;
   const long long M = (long long)d.B * d.H * d.W;
   dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((d.C_out + BN - 1) / BN));
@@ -341,6 +351,7 @@ cudaError_t launch_conv_simt(const dpp_conv_desc &d, const void *x, const void *
 }
 
 cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s) {
+  if (g.geglu) return cudaErrorNotSupported;
   dim3 grid((unsigned)((g.M + BM - 1) / BM), (unsigned)((g.N + BN - 1) / BN));
   if (g.ta == E_F32 && g.tb == E_F32 && g.to == E_F32)
     gemm_simt_kernel<float, float, float><<<grid, NT, 0, s>>>(g);

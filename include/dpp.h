@@ -92,33 +92,64 @@ typedef enum { DPP_F32 = 0, DPP_BF16 = 1 } dpp_dtype;
  *                   DistriFusion notes, Introduction para. 3). */
 typedef enum { DPP_HALO_STALE = 0, DPP_HALO_FRESH = 1, DPP_HALO_ZERO = 2 } dpp_halo;
 
-/* 3x3 conv, stride 1, zero padding 1, C_in -> C_out; halo: a dpp_halo. */
+/* 3x3 conv, stride 1, zero padding 1, C_in -> C_out; halo: a dpp_halo.
+ * accumulate != 0: y += the conv's result (y is read first: the residual
+ * addition of a ResNet block, done in place on the residual). */
 typedef struct {
   int B, H, W, C_in, C_out, P;
   dpp_dtype dtype;
   int halo;
+  int accumulate;
 } dpp_conv_desc;
+
+/* Activation applied after a GroupNorm's affine. */
+typedef enum { DPP_ACT_NONE = 0, DPP_ACT_SILU = 1 } dpp_act;
 
 /* GroupNorm over [B, H, W, C] with G groups of C/G consecutive channels.
  * band_local != 0: naive patch parallelism -- each band's statistics over
- * its own rows only (stats_prev is ignored). */
+ * its own rows only (stats_prev is ignored).
+ * act: a dpp_act applied to the output (DPP_ACT_SILU: y * sigmoid(y), the
+ * GroupNorm -> SiLU of a ResNet block); the statistics are those of x. */
 typedef struct {
   int B, H, W, C, G, P;
   float eps;
   dpp_dtype dtype;
   int band_local;
+  int act;
 } dpp_gn_desc;
 
 /* Attention over an H x W token grid (N = H*W), C = heads * head_dim.
  * n_ctx / c_ctx: text-context length and width (cross-attention only).
  * band_local != 0 (self-attention): naive patch parallelism -- a band's
- * queries attend over its own tokens only (kv_prev is ignored). */
+ * queries attend over its own tokens only (kv_prev is ignored).
+ * accumulate != 0: y += the attention's output (y is read first: the
+ * residual addition of a transformer block, in place on the residual). */
 typedef struct {
   int B, H, W, C, heads, head_dim, P;
   int n_ctx, c_ctx;
   dpp_dtype dtype;
   int band_local;
+  int accumulate;
 } dpp_attn_desc;
+
+/* LayerNorm over the C channels of each of T tokens. */
+typedef struct {
+  int T, C;
+  float eps;
+  dpp_dtype dtype;
+} dpp_ln_desc;
+
+/* y[M, N] = x[M, K] w^T + bias (torch Linear, w [N, K]).
+ * epilogue DPP_EPI_GEGLU: w is [2N, K] and bias [2N]; with h = x w^T + bias,
+ * y = h[:, :N] * GELU(h[:, N:]) (exact erf GELU: the gated feed-forward of a
+ * transformer block).  accumulate != 0: y += the result (y read first). */
+typedef enum { DPP_EPI_NONE = 0, DPP_EPI_GEGLU = 1 } dpp_epilogue;
+typedef struct {
+  int M, K, N;
+  dpp_dtype dtype;
+  int epilogue;
+  int accumulate;
+} dpp_linear_desc;
 
 /* ---------------------------------------------------------------------------
  * dpp_conv3x3 -- DistriConv2dPP (section 卷积层拆分 of the DistriFusion
@@ -297,6 +328,30 @@ size_t dpp_cfg_workspace_bytes(size_t n);
  * ------------------------------------------------------------------------- */
 dpp_status dpp_refresh_stale(const void *fresh, void *stale, size_t outer, size_t rows,
                              size_t row_bytes, int P, uint64_t patch_mask, dpp_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Per-token layers of the U-Net's transformer blocks.  The DistriFusion
+ * developer guide (sections 卷积层拆分, 注意力机制拆分, 归一化层拆分) replaces
+ * only the convolutions, the attention layers and the GroupNorms; the layers
+ * below act on one token at a time, so a band computes them on its own rows
+ * with no stale state.
+ *
+ * dpp_layernorm: y[t, c] = (x[t, c] - mean_t) / sqrt(var_t + eps) * gamma[c]
+ *   + beta[c], mean and biased variance over the C channels of token t.
+ *   x, y : [T, C] desc->dtype (bf16 or fp32); y may equal x.
+ *   gamma, beta : [C] fp32, both NULL for no affine.
+ *   Requires C a multiple of 8 (bf16) / 4 (fp32), C <= 8192.
+ *
+ * dpp_linear: see dpp_linear_desc.  x [M, K], y [M, N] bf16; w [N, K] (or
+ *   [2N, K] for DPP_EPI_GEGLU) bf16; bias fp32 or NULL.  Tensor cores;
+ *   requires DPP_BF16, K a multiple of 8, N a multiple of 64 (of 128 with
+ *   DPP_EPI_GEGLU); y must not overlap x or w.  DPP_ERR_UNSUPPORTED for
+ *   other types.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_layernorm(const dpp_ln_desc *desc, const void *x, const float *gamma,
+                         const float *beta, void *y, dpp_stream stream);
+dpp_status dpp_linear(const dpp_linear_desc *desc, const void *x, const void *w,
+                      const float *bias, void *y, dpp_stream stream);
 
 /* ---------------------------------------------------------------------------
  * Adaptive parallelism switching (the Hydiff summaries: gist.science,

@@ -172,6 +172,61 @@ def test_refresh_validation():
     assert f(A, Bp, 1, 8, 64, 4, patch_mask=0, stream=0, raise_on_error=False) == dpp.DPP_OK
 
 
+def ln(**kw):
+    d = dict(T=64, C=640, eps=1e-5, dtype=dpp.DPP_BF16)
+    d.update(kw)
+    return dpp.dpp_ln_desc(**d)
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(C=12), {}, dpp.DPP_ERR_INVALID_ARG),            # bf16 needs C % 8 == 0
+    (dict(T=0), {}, dpp.DPP_ERR_INVALID_ARG),
+    (dict(C=4096), {}, dpp.DPP_ERR_UNSUPPORTED),          # more than 256 vectors a token
+    (dict(dtype=dpp.DPP_F32, C=2048), {}, dpp.DPP_ERR_UNSUPPORTED),
+    (dict(eps=-1.0), {}, dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(beta=None), dpp.DPP_ERR_INVALID_ARG),        # gamma without beta
+    ({}, dict(x=A + 4), dpp.DPP_ERR_ALIGN),
+    ({}, dict(y=A + 64), dpp.DPP_ERR_ALIAS),               # partial overlap (y == x is fine)
+    ({}, dict(y=Cp + 16), dpp.DPP_ERR_ALIAS),              # output over gamma
+])
+def test_layernorm_validation(kw, ptrs, want):
+    p = dict(x=A, gamma=Cp, beta=Dp, y=Bp)
+    p.update(ptrs)
+    before = dpp.dpp_launch_count()
+    st = dpp.dpp_layernorm(ln(**kw), p["x"], p["gamma"], p["beta"], p["y"], stream=0,
+                           raise_on_error=False)
+    assert st == want and dpp.dpp_launch_count() == before
+
+
+def lin(**kw):
+    d = dict(M=256, K=640, N=640, dtype=dpp.DPP_BF16, epilogue=dpp.DPP_EPI_NONE, accumulate=0)
+    d.update(kw)
+    return dpp.dpp_linear_desc(**d)
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(dtype=dpp.DPP_F32), {}, dpp.DPP_ERR_UNSUPPORTED),
+    (dict(N=32), {}, dpp.DPP_ERR_INVALID_ARG),             # N % 64
+    (dict(K=12), {}, dpp.DPP_ERR_INVALID_ARG),             # K % 8
+    (dict(M=0), {}, dpp.DPP_ERR_INVALID_ARG),
+    (dict(epilogue=5), {}, dpp.DPP_ERR_INVALID_ARG),
+    (dict(dtype=7), {}, dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(x=0), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(w=Cp + 8), dpp.DPP_ERR_ALIGN),
+    ({}, dict(y=A + 1024), dpp.DPP_ERR_ALIAS),             # output over x
+    ({}, dict(y=Cp + 1024), dpp.DPP_ERR_ALIAS),            # output over w
+    (dict(epilogue=dpp.DPP_EPI_GEGLU), dict(y=Cp + 640 * 640 * 2 + 64),
+     dpp.DPP_ERR_ALIAS),                                   # output over the gate rows
+])
+def test_linear_validation(kw, ptrs, want):
+    p = dict(x=A, w=Cp, bias=None, y=Bp)
+    p.update(ptrs)
+    before = dpp.dpp_launch_count()
+    st = dpp.dpp_linear(lin(**kw), p["x"], p["w"], p["bias"], p["y"], stream=0,
+                        raise_on_error=False)
+    assert st == want and dpp.dpp_launch_count() == before
+
+
 def test_error_raises_with_status_name():
     with pytest.raises(dpp.DppError, match="DPP_ERR_INVALID_ARG"):
         dpp.dpp_conv3x3(conv(H=9), A, Bp, Cp, None, Dp, stream=0)

@@ -186,3 +186,75 @@ def guidance_maps(shape, index: int):
 def to_f64(t: torch.Tensor):
     """Exact upcast of a CPU tensor (fp32 or bf16) to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+# ------------------------------------------------------------ block chain
+@dataclasses.dataclass(frozen=True)
+class ChainShape:
+    """One U-Net level stepped as a ResNet block + transformer block:
+    latent B x H x W x C in P bands, G GroupNorm groups, `heads` heads of
+    C / heads, text context n_ctx x c_ctx, feed-forward width ff_mult * C."""
+    name: str
+    index: int
+    B: int
+    H: int
+    W: int
+    C: int
+    heads: int
+    P: int
+    G: int = 32
+    n_ctx: int = 77
+    c_ctx: int = 2048
+    ff_mult: int = 4
+    stale_scale: float = 0.05
+
+
+CHAINS = {
+    c.name: c
+    for c in [
+        # small enough for the fp64 oracle, several tiles of every kernel
+        ChainShape("chain_small", 6, 2, 16, 16, 320, 5, 4, n_ctx=77, c_ctx=256),
+        # SDXL at 3840px, level 2 of the down path (latent 480 -> 240 x 240 x 640)
+        ChainShape("sdxl_3840_level2", 7, 2, 240, 240, 640, 10, 8),
+    ]
+}
+
+
+def chain_weights(ch: ChainShape, dtype: str = "bf16"):
+    """Weights of the chain in torch layouts (conv [C, C, 3, 3], Linear [out,
+    in]; ff1 is [2 F, C]: value rows then gate rows).  Weights ~ N(0, 1/fan_in)
+    in `dtype`; biases ~ 0.1 N(0, 1), affine gains 1 + 0.1 N(0, 1) and shifts
+    0.1 N(0, 1), all fp32.  Seeds 1000 * index + 100 + k, k the name's rank."""
+    C, F, X = ch.C, ch.ff_mult * ch.C, ch.c_ctx
+    spec = [
+        ("gn1_g", (C,), "gain"), ("gn1_b", (C,), "shift"), ("conv1_w", (C, C, 3, 3), 9 * C),
+        ("conv1_b", (C,), "shift"), ("gn2_g", (C,), "gain"), ("gn2_b", (C,), "shift"),
+        ("conv2_w", (C, C, 3, 3), 9 * C), ("conv2_b", (C,), "shift"),
+        ("gn_g", (C,), "gain"), ("gn_b", (C,), "shift"), ("pi_w", (C, C), C),
+        ("pi_b", (C,), "shift"), ("ln1_g", (C,), "gain"), ("ln1_b", (C,), "shift"),
+        ("wq", (C, C), C), ("wk", (C, C), C), ("wv", (C, C), C), ("wo", (C, C), C),
+        ("ln2_g", (C,), "gain"), ("ln2_b", (C,), "shift"), ("xq", (C, C), C),
+        ("xk", (C, X), X), ("xv", (C, X), X), ("xo", (C, C), C),
+        ("ln3_g", (C,), "gain"), ("ln3_b", (C,), "shift"), ("ff1_w", (2 * F, C), C),
+        ("ff1_b", (2 * F,), "shift"), ("ff2_w", (C, F), F), ("ff2_b", (C,), "shift"),
+        ("po_w", (C, C), C), ("po_b", (C,), "shift"),
+    ]
+    out = {}
+    for k, (name, shape, kind) in enumerate(spec):
+        seed = 1000 * ch.index + 100 + k
+        if kind == "gain":
+            out[name] = normal(shape, seed, std=0.1, mean=1.0)
+        elif kind == "shift":
+            out[name] = normal(shape, seed, std=0.1)
+        else:
+            out[name] = normal(shape, seed, std=float(kind) ** -0.5, dtype=dtype)
+    return out
+
+
+def chain_inputs(ch: ChainShape, steps: int, dtype: str = "bf16"):
+    """Level inputs for steps 0..steps (F_s = F_{s-1} + stale_scale N(0, 1))
+    and the text context, both in `dtype`."""
+    xs = activation_steps((ch.B, ch.H, ch.W, ch.C), ch.index, steps, ch.stale_scale, dtype,
+                          tensor_id=T_FRESH)
+    ctx = normal((ch.B, ch.n_ctx, ch.c_ctx), seed_of(ch.index, 0, T_CTX), dtype=dtype)
+    return xs, ctx
