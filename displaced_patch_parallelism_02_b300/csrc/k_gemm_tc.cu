@@ -13,7 +13,10 @@
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
 //               (M = 128, N = BN, K = 16 per instruction), fp32 accumulators
 //               double-buffered in TMEM (2 x BN columns);
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, convert, store.
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, + bias (a per-warp
+//               shared-memory copy of the tile's), + the residual in out0
+//               (prefetched before the accumulator is ready), convert, store;
+//               or the gated-GELU epilogue (value * GELU(gate)).
 // Tiles are ordered n-fastest so CTAs running together share A rows in L2.
 #include "tc_common.cuh"
 
@@ -204,14 +207,48 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {  // ------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane;
+    // this warp's copy of the tile's bias (gated GELU: value bias, then gate bias)
+    float *bias_s = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + 512) + q * BN;
+    constexpr int PRE = BN <= 128 ? BN / 8 : 1;  // residual vectors a thread prefetches
     int it = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
-      tc_fence_after();
       const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
       const int m = m0 + row;
+      // Before the accumulator is ready, so that neither latency lands after
+      // the MMA: the tile's bias into this warp's slice, and (128-column
+      // tiles) the loads of the residual row already in out0.
+      if (p.bias) {
+        __syncwarp();  // this warp's reads of the previous tile's slice are done
+        for (int j = lane; j < BN; j += 32) {
+          float b = 0.f;
+          if (p.geglu) {
+            const int jj = j < BN / 2 ? j : j - BN / 2;
+            if (n0 / 2 + jj < p.N) b = __ldg(p.bias + (j < BN / 2 ? 0 : p.N) + n0 / 2 + jj);
+          } else if (n0 + j < p.N && n0 + j < p.split) {
+            b = __ldg(p.bias + n0 + j);
+          }
+          bias_s[j] = b;
+        }
+        __syncwarp();
+      }
+      uint4 pre[PRE];
+      if constexpr (BN <= 128) {
+        const bool pre_acc = p.accumulate && !p.geglu && m < p.M;
+#pragma unroll
+        for (int k = 0; k < PRE; ++k) {
+          const int n = n0 + 8 * k;
+          pre[k] = pre_acc && n < p.N && n < p.split
+                       ? *reinterpret_cast<const uint4 *>(
+                             reinterpret_cast<const uint16_t *>(p.out0) + (size_t)m * p.ld0 + n)
+                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // every lane leaves together (a lane that timed out has set the abort flag)
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)))
+        break;
+      tc_fence_after();
       if (p.geglu) {
         // value columns [0, BN/2) and gate columns [BN/2, BN) of the tile:
         // out[n0/2 + j] = (value_j + b_j) * GELU(gate_j + b_{N + j})
@@ -221,15 +258,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32;
           tmem_ld32(ta, rv);
           tmem_ld32(ta + BN / 2, rg);
-          tmem_wait_ld();
           const int n = n0 / 2 + c * 32;
-          if (m < p.M && n < p.N) {
-            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out0) + (size_t)m * p.ld0 + n;
-            uint4 res[4];
+          __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out0) + (size_t)m * p.ld0 + n;
+          const bool in = m < p.M && n < p.N;
+          uint4 res[4];  // loads in flight while the accumulator is read
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              res[v] = p.accumulate ? reinterpret_cast<const uint4 *>(dst)[v]
-                                    : make_uint4(0u, 0u, 0u, 0u);
+          for (int v = 0; v < 4; ++v)
+            res[v] = in && p.accumulate ? reinterpret_cast<const uint4 *>(dst)[v]
+                                        : make_uint4(0u, 0u, 0u, 0u);
+          tmem_wait_ld();
+          if (in) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
@@ -240,10 +278,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 float f[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                  const int k = v * 8 + 2 * e + h, col = n + k;
-                  const float a = __uint_as_float(rv[k]) + (p.bias ? __ldg(p.bias + col) : 0.f);
+                  const int k = v * 8 + 2 * e + h;
+                  const float a = __uint_as_float(rv[k]) + (p.bias ? bias_s[c * 32 + k] : 0.f);
                   const float g =
-                      __uint_as_float(rg[k]) + (p.bias ? __ldg(p.bias + p.N + col) : 0.f);
+                      __uint_as_float(rg[k]) + (p.bias ? bias_s[BN / 2 + c * 32 + k] : 0.f);
                   f[h] = a * (0.5f * g * (1.f + erff(g * 0.70710678118654752f)));
                 }
                 f[0] += __uint_as_float(rw[e] << 16);
@@ -259,25 +297,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) mbar_arrive(&tempty[acc]);
         continue;
       }
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
-        tmem_wait_ld();
         const int n = n0 + c * 32;
-        if (m < p.M && n < p.N) {
-          uint4 *dst;
-          const bool first = n < p.split;
-          if (first)
-            dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out0) +
-                                            (size_t)m * p.ld0 + n);
-          else
-            dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out1) +
-                                            (size_t)m * p.ld1 + (n - p.split));
-          const bool acc_in = first && p.accumulate;
-          uint4 res[4];  // the residual already in out0, all four loads in flight
+        const bool in = m < p.M && n < p.N;
+        const bool first = n < p.split;
+        uint4 *dst = first ? reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out0) +
+                                                       (size_t)m * p.ld0 + n)
+                           : reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out1) +
+                                                       (size_t)m * p.ld1 + (n - p.split));
+        const bool acc_in = first && p.accumulate;
+        uint4 res[4];  // the residual already in out0
+        if constexpr (BN <= 128) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) res[v] = acc_in ? dst[v] : make_uint4(0u, 0u, 0u, 0u);
+          for (int v = 0; v < 4; ++v) res[v] = pre[c * 4 + v];
+        } else {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            res[v] = in && acc_in ? dst[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        tmem_wait_ld();
+        if (in) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 o;
@@ -285,12 +327,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int col = n + v * 8 + 2 * e;
-              float a = __uint_as_float(r[v * 8 + 2 * e]);
-              float b = __uint_as_float(r[v * 8 + 2 * e + 1]);
-              if (first && p.bias) {
-                a += __ldg(p.bias + col);
-                b += __ldg(p.bias + col + 1);
+              const int k = v * 8 + 2 * e;
+              float a = __uint_as_float(r[k]);
+              float b = __uint_as_float(r[k + 1]);
+              if (p.bias) {  // zero outside out0's columns
+                a += bias_s[c * 32 + k];
+                b += bias_s[c * 32 + k + 1];
               }
               if (acc_in) {  // out0 is bf16 or fp16, as the output
                 if (p.out_f16) {
@@ -345,7 +387,9 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
   GemmTcParams p{g.M, g.N, g.K, g.b_rows, g.out0, g.ld0, g.split, g.out1, g.ld1,
                  g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, (n_cols + BN - 1) / BN, status,
                  g.bias, g.accumulate ? 1 : 0, g.geglu ? 1 : 0};
-  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512;
+  // stages, 1024-byte alignment slack, barriers, the epilogue warps' bias slices
+  constexpr size_t smem =
+      (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512 + 4 * BN * sizeof(float);
   auto k = gemm_tc_kernel<BN, STAGES, IN_BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -118,9 +118,11 @@ __device__ __forceinline__ bool gn_bar_wait(uint64_t *bar, uint32_t parity, int 
 }
 
 // The activation that may follow the affine (DPP_ACT_SILU: x * sigmoid(x),
-// the GroupNorm -> SiLU of a ResNet block).
+// the GroupNorm -> SiLU of a ResNet block).  The exponent is clamped at 80 so
+// that 1 + e stays far below 2^126, the range of the fast divide; below
+// x = -80 both the clamped and the exact value are under 1e-33 in size.
 __device__ __forceinline__ float gn_act(float x, int act) {
-  return act == DPP_ACT_SILU ? x / (1.f + __expf(-x)) : x;
+  return act == DPP_ACT_SILU ? __fdividef(x, 1.f + __expf(fminf(-x, 80.f))) : x;
 }
 
 template <typename T>

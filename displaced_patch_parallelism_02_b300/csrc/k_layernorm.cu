@@ -67,21 +67,14 @@ layernorm_kernel(const T *x, T *y, const float *__restrict__ gamma,
   constexpr int VE = LnVec<T>::N;
   const int lane = threadIdx.x % 32;
   const int nvec = C / VE;
-  // gamma/beta slices live in registers for up to 4 vectors per lane; wider
-  // tokens re-read them from L1 per token, which keeps 2 CTAs per SM resident
-  constexpr bool kRegAffine = V <= 4;
-  constexpr int VA = kRegAffine ? V : 1;
-  float ga[VA][VE], be[VA][VE];
-#pragma unroll
-  for (int i = 0; i < VA; ++i) {
-    const int v = lane + 32 * i;
-#pragma unroll
-    for (int e = 0; e < VE; ++e) {
-      const bool in = v < nvec;
-      ga[i][e] = in && gamma ? gamma[v * VE + e] : 1.f;
-      be[i][e] = in && beta ? beta[v * VE + e] : 0.f;
-    }
+  // gamma and beta for the whole token, once per CTA, in shared memory (the
+  // registers go to keeping more tokens' loads in flight)
+  extern __shared__ float ln_aff[];  // [2][C]
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    ln_aff[c] = gamma ? gamma[c] : 1.f;
+    ln_aff[C + c] = beta ? beta[c] : 0.f;
   }
+  __syncthreads();
   const float inv_c = 1.f / (float)C;
   const int warps = gridDim.x * kLnWarps;
   for (int t = blockIdx.x * kLnWarps + threadIdx.x / 32; t < tokens; t += warps) {
@@ -119,16 +112,19 @@ layernorm_kernel(const T *x, T *y, const float *__restrict__ gamma,
     for (int i = 0; i < V; ++i) {
       const int v = lane + 32 * i;
       if (v < nvec) {
-        float o[VE];
-        if constexpr (kRegAffine) {
+        // 16-byte shared loads of the vector's gains and shifts (a lane's
+        // VE floats are contiguous: at most a 2-way bank conflict)
+        float ga[VE], be[VE];
 #pragma unroll
-          for (int e = 0; e < VE; ++e) o[e] = fmaf((f[i][e] - mean) * rstd, ga[i][e], be[i][e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < VE; ++e)
-            o[e] = fmaf((f[i][e] - mean) * rstd, gamma ? __ldg(gamma + v * VE + e) : 1.f,
-                        beta ? __ldg(beta + v * VE + e) : 0.f);
+        for (int q = 0; q < VE / 4; ++q) {
+          const float4 g4 = reinterpret_cast<const float4 *>(ln_aff + v * VE)[q];
+          const float4 b4 = reinterpret_cast<const float4 *>(ln_aff + C + v * VE)[q];
+          ga[4 * q] = g4.x; ga[4 * q + 1] = g4.y; ga[4 * q + 2] = g4.z; ga[4 * q + 3] = g4.w;
+          be[4 * q] = b4.x; be[4 * q + 1] = b4.y; be[4 * q + 2] = b4.z; be[4 * q + 3] = b4.w;
         }
+        float o[VE];
+#pragma unroll
+        for (int e = 0; e < VE; ++e) o[e] = fmaf((f[i][e] - mean) * rstd, ga[e], be[e]);
         __stcs(reinterpret_cast<uint4 *>(yr) + v, LnVec<T>::pack(o));
       }
     }
@@ -142,13 +138,15 @@ cudaError_t run_ln(const dpp_ln_desc &d, const void *x, const float *gamma, cons
   int dev = 0, sms = 148, per_sm = 1;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kLnWarps * 32, 0);
+  const size_t smem = (size_t)2 * d.C * sizeof(float);
+  cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kLnWarps * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const long long need = (d.T + kLnWarps - 1) / kLnWarps;
   const long long full = (long long)sms * per_sm;
   const int grid = (int)(need < full ? need : full);
-  k<<<grid, kLnWarps * 32, 0, s>>>((const T *)x, (T *)y, gamma, beta, d.T, d.C, d.eps);
+  k<<<grid, kLnWarps * 32, smem, s>>>((const T *)x, (T *)y, gamma, beta, d.T, d.C, d.eps);
   return cudaGetLastError();
 }
 
