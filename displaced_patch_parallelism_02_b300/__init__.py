@@ -45,6 +45,13 @@ DPP_ACT_SILU = 1
 DPP_EPI_NONE = 0
 DPP_EPI_GEGLU = 1
 
+DPP_OP_CONV3X3 = 0
+DPP_OP_GROUPNORM = 1
+DPP_OP_SELF_ATTN = 2
+DPP_OP_CROSS_ATTN = 3
+DPP_OP_CFG_COMBINE = 4
+DPP_OP_REFRESH_STALE = 5
+
 
 class DppError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -123,6 +130,7 @@ _SIGNATURES = {
     "dpp_version": (ctypes.c_int, []),
     "dpp_launch_count": (ctypes.c_uint64, []),
     "dpp_set_attn_core_events": (None, [_vp, _vp]),
+    "dpp_workspace_bytes": (_sz, [ctypes.c_int, _vp]),
     "dpp_layernorm": (_st, [ctypes.POINTER(dpp_ln_desc), _vp, _vp, _vp, _vp, _vp]),
     "dpp_linear": (_st, [ctypes.POINTER(dpp_linear_desc), _vp, _vp, _vp, _vp, _vp]),
     "dpp_switch_init": (None, [ctypes.POINTER(dpp_switch_state), ctypes.c_double,
@@ -215,6 +223,16 @@ def dpp_groupnorm_apply(desc: dpp_gn_desc, x, stats_prev, gn_sums, stats_next, g
                                           _ptr(gn_sums), _ptr(stats_next), _ptr(gamma),
                                           _ptr(beta), _ptr(y), _stream(stream)),
                   "dpp_groupnorm_apply", raise_on_error)
+
+
+def dpp_workspace_bytes(op: int, desc) -> int:
+    """desc: the op's descriptor (a ctypes structure) or, for
+    DPP_OP_CFG_COMBINE, the element count n."""
+    if isinstance(desc, int):
+        arg = ctypes.byref(ctypes.c_size_t(desc))
+    else:
+        arg = ctypes.byref(desc)
+    return lib.dpp_workspace_bytes(int(op), ctypes.cast(arg, _vp))
 
 
 def dpp_layernorm(desc: dpp_ln_desc, x, gamma, beta, y, stream=None,

@@ -435,6 +435,22 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
                             (int)nt, s));
 }
 
+size_t dpp_workspace_bytes(int op, const void *desc) {
+  if (!desc) return 0;
+  switch (op) {
+    case DPP_OP_GROUPNORM:
+      return dpp_groupnorm_workspace_bytes(static_cast<const dpp_gn_desc *>(desc));
+    case DPP_OP_SELF_ATTN:
+      return dpp_self_attn_workspace_bytes(static_cast<const dpp_attn_desc *>(desc));
+    case DPP_OP_CROSS_ATTN:
+      return dpp_cross_attn_workspace_bytes(static_cast<const dpp_attn_desc *>(desc));
+    case DPP_OP_CFG_COMBINE:
+      return dpp_cfg_workspace_bytes(*static_cast<const size_t *>(desc));
+    default:
+      return 0;
+  }
+}
+
 // ---------------------------------------------------- per-token layers
 dpp_status dpp_layernorm(const dpp_ln_desc *d, const void *x, const float *gamma,
                          const float *beta, void *y, dpp_stream stream) {

@@ -354,6 +354,24 @@ dpp_status dpp_linear(const dpp_linear_desc *desc, const void *x, const void *w,
                       const float *bias, void *y, dpp_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * dpp_workspace_bytes -- the workspace any entry point needs, by op: the
+ * per-op queries above behind one call.  desc points to the op's descriptor
+ * (dpp_gn_desc for DPP_OP_GROUPNORM, dpp_attn_desc for the attention ops,
+ * a size_t element count for DPP_OP_CFG_COMBINE).  Ops that need no
+ * workspace (conv, refresh, LayerNorm, linear, the one-pass GroupNorm)
+ * return 0; an invalid descriptor or op returns 0 as well.
+ * ------------------------------------------------------------------------- */
+typedef enum {
+  DPP_OP_CONV3X3 = 0,
+  DPP_OP_GROUPNORM = 1,
+  DPP_OP_SELF_ATTN = 2,
+  DPP_OP_CROSS_ATTN = 3,
+  DPP_OP_CFG_COMBINE = 4,
+  DPP_OP_REFRESH_STALE = 5
+} dpp_op;
+size_t dpp_workspace_bytes(int op, const void *desc);
+
+/* ---------------------------------------------------------------------------
  * Adaptive parallelism switching (the Hydiff summaries: gist.science,
  * section 自适应并行切换; Avetisyan, "Адаптивное переключение").  Host-side
  * state machine over the per-step denoising discrepancy d (rel-MAE of the

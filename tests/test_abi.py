@@ -254,3 +254,19 @@ def test_static_groupnorm_rejects_oversize_scratch_on_the_host():
     assert st == dpp.DPP_ERR_WORKSPACE and dpp.dpp_launch_count() == before
     assert dpp.dpp_groupnorm_static(gn(C=30), A, None, Ep, None, None, Dp, stream=0,
                                     raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+
+
+def test_generic_workspace_query_matches_the_per_op_queries():
+    g = gn()
+    assert dpp.dpp_workspace_bytes(dpp.DPP_OP_GROUPNORM, g) == dpp.dpp_groupnorm_workspace_bytes(g)
+    a = attn()
+    assert dpp.dpp_workspace_bytes(dpp.DPP_OP_SELF_ATTN, a) == dpp.dpp_self_attn_workspace_bytes(a)
+    x = attn(n_ctx=77, c_ctx=2048)
+    assert dpp.dpp_workspace_bytes(dpp.DPP_OP_CROSS_ATTN, x) == \
+        dpp.dpp_cross_attn_workspace_bytes(x)
+    assert dpp.dpp_workspace_bytes(dpp.DPP_OP_CFG_COMBINE, 921600) == \
+        dpp.dpp_cfg_workspace_bytes(921600) > 0
+    assert dpp.dpp_workspace_bytes(dpp.DPP_OP_CONV3X3, conv()) == 0
+    assert dpp.dpp_workspace_bytes(dpp.DPP_OP_REFRESH_STALE, conv()) == 0
+    assert dpp.dpp_workspace_bytes(99, g) == 0
+    assert dpp.dpp_workspace_bytes(dpp.DPP_OP_GROUPNORM, gn(C=30)) == 0
