@@ -405,7 +405,8 @@ def time_chain(dev, steps, warmup=2):
     with displaced patch parallelism at 3840px: latent 2 x 240 x 240 x 640 in
     8 bands, 10 heads, text context 77 x 2048.  Times `steps` displaced steps
     back to back, then the same number again with an event pair around every
-    op; returns the per-step figures."""
+    op, then the two guidance branches as chains of batch 1 run serially and
+    on two streams; returns the per-step figures."""
     import displaced_patch_parallelism_02_b300 as dpp
     from displaced_patch_parallelism_02_b300.chain import OPS, BlockChain
     ch = wl.CHAINS["sdxl_3840_level2"]
@@ -447,13 +448,35 @@ def time_chain(dev, steps, warmup=2):
         op_ms[n] += e1.elapsed_time(e2) / max(steps, 1)
     ok = dpp.dpp_device_status() == dpp.DPP_OK and bool(torch.isfinite(x.float()).all())
     flop = chain.flops()
-    del chain, wts, x, ctx
+    del chain
+    torch.cuda.empty_cache()
+    # the guided pair as two branches of batch 1 (condition-based partition):
+    # serially on one stream, and on two streams (the parallel stage)
+    from displaced_patch_parallelism_02_b300.chain import BranchPair
+    pair = BranchPair(ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx, wts, dev,
+                      ff_mult=ch.ff_mult)
+    xb = [x[b:b + 1].contiguous() for b in range(2)]
+    cb = [ctx[b:b + 1].contiguous() for b in range(2)]
+    sched = {}
+    for name, par in (("branches_serial", False), ("branches_two_stream", True)):
+        for _ in range(max(warmup, 1)):
+            pair.step(xb, cb, par, stream=s)
+        torch.cuda.synchronize(dev)
+        a.record(s)
+        for _ in range(steps):
+            pair.step(xb, cb, par, stream=s)
+        b.record(s)
+        torch.cuda.synchronize(dev)
+        sched[name] = a.elapsed_time(b) / max(steps, 1)
+    ok = ok and dpp.dpp_device_status() == dpp.DPP_OK
+    del pair, wts, x, ctx, xb, cb
     torch.cuda.empty_cache()
     return {"workload": ch.name, "latent": [ch.B, ch.H, ch.W, ch.C], "P": ch.P,
             "heads": ch.heads, "context": [ch.n_ctx, ch.c_ctx], "steps": steps,
             "ms_per_step": ms, "tflops": flop / (ms / 1e3) / 1e12, "step_flop": flop,
             "launches_per_step": launches, "ok": ok,
-            "ops_ms": {n: round(v, 4) for n, v in op_ms.items()}}
+            "ops_ms": {n: round(v, 4) for n, v in op_ms.items()},
+            "schedules_ms_per_step": {"batched": ms, **sched}}
 
 
 def cpu_cores():

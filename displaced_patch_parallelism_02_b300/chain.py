@@ -173,3 +173,40 @@ class BlockChain:
                                           stream=s),
            {"x": self.h}, tok)
         self.k += 1
+
+
+class BranchPair:
+    """Hydiff's condition-based partition of a guided step on one GPU (the
+    gist.science summary of Hybridiff, section 基于条件的数据划分): the
+    conditional and the unconditional branch as two chains of batch 1, each
+    with displaced states of its own.  In the serial stages (warm-up and fully
+    connecting, section 自适应并行切换) the branches run one after the other on
+    the caller's stream; in the parallel stage each runs on a stream of its
+    own, joined by an event, as two devices would run them.  The arithmetic
+    of a branch does not depend on the schedule."""
+
+    def __init__(self, H, W, C, heads, P, G, n_ctx, c_ctx, weights, device, **kw):
+        dev = torch.device(device)
+        self.branches = [BlockChain(1, H, W, C, heads, P, G, n_ctx, c_ctx, weights, dev, **kw)
+                         for _ in range(2)]
+        self.side = torch.cuda.Stream(dev)
+        self.forked, self.joined = torch.cuda.Event(), torch.cuda.Event()
+
+    def flops(self):
+        return sum(b.flops() for b in self.branches)
+
+    def step(self, xs, ctxs, parallel, stream=None):
+        """xs, ctxs: per branch ([1, H, W, C] and [1, n_ctx, c_ctx] bf16; x is
+        updated in place); parallel: the stage the switching controller chose
+        (DPP_STAGE_PARALLEL) runs the branches on two streams."""
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if not parallel:
+            for b in range(2):
+                self.branches[b].step(xs[b], ctxs[b], stream=main)
+            return
+        self.forked.record(main)
+        self.side.wait_event(self.forked)
+        self.branches[0].step(xs[0], ctxs[0], stream=main)
+        self.branches[1].step(xs[1], ctxs[1], stream=self.side)
+        self.joined.record(self.side)
+        main.wait_event(self.joined)

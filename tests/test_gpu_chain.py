@@ -305,3 +305,37 @@ def test_chain_launches_only_library_kernels_and_repeats(cuda_device):
         assert dpp.dpp_launch_count() - n0 == 24
         outs.append(G.f64(x))
     check(outs[1], outs[0], BF16, "repeated input, displaced vs synchronous step")
+
+
+def test_branch_schedules_agree(cuda_device):
+    """Hydiff's condition-based partition on one GPU: the two branches as
+    chains of batch 1, serially or on two streams, three steps each (the
+    synchronous one and two displaced).  Serial and two-stream results are
+    bit-identical; both match the batched chain at the parity bar."""
+    from displaced_patch_parallelism_02_b300.chain import BranchPair
+    ch = CH
+    wts = chain_device_weights(wl.chain_weights(ch))
+    xs, ctx = wl.chain_inputs(ch, 2)
+    ctx_d = ctx.to("cuda")
+    args = (ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx, wts, "cuda")
+    batched = BlockChain(ch.B, *args)
+    ref = []
+    for s in range(3):
+        x = xs[s].to("cuda", copy=True)
+        batched.step(x, ctx_d)
+        ref.append(x.cpu())
+    ctxs = [ctx_d[b:b + 1].contiguous() for b in range(2)]
+    runs = {}
+    for name, pattern in (("serial", (False, False, False)), ("two_stream", (False, True, True))):
+        pair = BranchPair(*args)
+        outs = []
+        for s, par in enumerate(pattern):
+            xb = [xs[s][b:b + 1].to("cuda", copy=True) for b in range(2)]
+            pair.step(xb, ctxs, par)
+            torch.cuda.synchronize()
+            outs.append(torch.cat(xb).cpu())
+        runs[name] = outs
+    assert dpp.dpp_device_status() == dpp.DPP_OK
+    for s in range(3):
+        assert torch.equal(runs["serial"][s], runs["two_stream"][s]), s
+        check(G.f64(runs["two_stream"][s]), G.f64(ref[s]), BF16, f"branches vs batched, step {s}")
