@@ -492,6 +492,22 @@ def cpu_cores():
 
 
 # ------------------------------------------------------------------ main
+def max_over_ranks(pg, ms, device):
+    """The slowest rank's time (every rank returns the same value); ms as is
+    when there is no process group."""
+    if pg is None:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_step_per_rank, world_size, steps, ms):
+    """Throughput of the whole job: the work every rank did over the slowest
+    rank's time (the replicas are independent and equal in size)."""
+    return flop_per_step_per_rank * world_size * steps / (ms / 1e3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -588,13 +604,9 @@ def main():
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, t_start.elapsed_time(t_end), dev)
     ms_step = total_ms / K
-    value = model["step_flop"] * ws * K / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(model["step_flop"], ws, K, total_ms)
 
     op_ms = {op: sum(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(K)) / K
              for j, op in enumerate(step.ops)}
@@ -685,17 +697,15 @@ def main():
         e1.record(cs)
         torch.cuda.synchronize(dev)
         step.select(0)
-        e2e_ms = e0.elapsed_time(e1)
-        if pg:
-            t = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e_val = model["step_flop"] * ws * K / (e2e_ms / 1e3) / 1e12
+        e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+        e2e_val = whole_job_tflops(model["step_flop"], ws, K, e2e_ms)
 
     chain = None
     if not args.no_chain and K > 0:
         chain = time_chain(dev, K)
-        chain["frac_of_sustained_bf16"] = chain["tflops"] / sus
+        chain["ms_per_step"] = max_over_ranks(pg, chain["ms_per_step"], dev)
+        chain["tflops"] = whole_job_tflops(chain["step_flop"], ws, 1, chain["ms_per_step"])
+        chain["frac_of_sustained_bf16"] = chain["tflops"] / (sus * ws)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
