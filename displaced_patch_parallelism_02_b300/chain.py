@@ -45,6 +45,34 @@ OPS = ("gn1", "conv1", "gn2", "conv2", "gn", "proj_in", "ln1", "attn1", "ln2", "
        "ff1", "ff2", "proj_out")
 
 
+def weight_shapes(C, F, c_ctx):
+    """Expected shape of every weight (conv weights channels-last)."""
+    shapes = {"conv1_w": (C, 3, 3, C), "conv2_w": (C, 3, 3, C), "pi_w": (C, C), "po_w": (C, C),
+              "wq": (C, C), "wk": (C, C), "wv": (C, C), "wo": (C, C), "xq": (C, C),
+              "xk": (C, c_ctx), "xv": (C, c_ctx), "xo": (C, C), "ff1_w": (2 * F, C),
+              "ff1_b": (2 * F,), "ff2_w": (C, F)}
+    for k in RESNET_WEIGHTS + TRANSFORMER_WEIGHTS:
+        shapes.setdefault(k, (C,))
+    return shapes
+
+
+def check_weights(weights, C, F, c_ctx, dev):
+    """The library reads weights through raw pointers, so their shapes,
+    types, device and layout are checked here once, on the host."""
+    shapes = weight_shapes(C, F, c_ctx)
+    missing = [k for k in shapes if k not in weights]
+    if missing:
+        raise ValueError(f"missing weights: {missing}")
+    for k, shape in shapes.items():
+        t = weights[k]
+        want = torch.float32 if len(shape) == 1 else torch.bfloat16
+        if tuple(t.shape) != shape or t.dtype != want or t.device != dev or \
+                not t.is_contiguous():
+            raise ValueError(f"weight {k}: want {shape} {want} contiguous on {dev}, got "
+                             f"{tuple(t.shape)} {t.dtype} on {t.device}")
+    return weights
+
+
 class BlockChain:
     """Buffers, states and the call sequence of one displaced step of the
     chain.  ``weights`` maps the names in RESNET_WEIGHTS and
@@ -55,8 +83,8 @@ class BlockChain:
                  ff_mult=4, eps_gn_res=1e-5, eps_gn_tf=1e-6, eps_ln=1e-5):
         self.B, self.H, self.W, self.C, self.P, self.G = B, H, W, C, P, G
         self.heads, self.n_ctx, self.c_ctx, self.F = heads, n_ctx, c_ctx, ff_mult * C
-        self.w = weights
         dev = torch.device(device)
+        self.w = check_weights(weights, C, self.F, c_ctx, dev)
         bf = torch.bfloat16
         N, M = H * W, B * H * W
         self.M = M

@@ -270,3 +270,22 @@ def test_generic_workspace_query_matches_the_per_op_queries():
     assert dpp.dpp_workspace_bytes(dpp.DPP_OP_REFRESH_STALE, conv()) == 0
     assert dpp.dpp_workspace_bytes(99, g) == 0
     assert dpp.dpp_workspace_bytes(dpp.DPP_OP_GROUPNORM, gn(C=30)) == 0
+
+
+def test_block_chain_checks_weight_shapes_on_the_host():
+    import torch
+    from displaced_patch_parallelism_02_b300 import chain
+    C, F, X = 64, 256, 32
+    shapes = chain.weight_shapes(C, F, X)
+    w = {k: torch.zeros(s, dtype=torch.float32 if len(s) == 1 else torch.bfloat16)
+         for k, s in shapes.items()}
+    assert chain.check_weights(w, C, F, X, torch.device("cpu")) is w
+    bad = dict(w, ff1_w=torch.zeros((F, C), dtype=torch.bfloat16))  # gate rows missing
+    with pytest.raises(ValueError, match="ff1_w"):
+        chain.check_weights(bad, C, F, X, torch.device("cpu"))
+    with pytest.raises(ValueError, match="missing"):
+        chain.check_weights({k: v for k, v in w.items() if k != "wo"}, C, F, X,
+                            torch.device("cpu"))
+    bad = dict(w, conv1_w=torch.zeros((C, C, 3, 3), dtype=torch.bfloat16))  # not channels-last
+    with pytest.raises(ValueError, match="conv1_w"):
+        chain.check_weights(bad, C, F, X, torch.device("cpu"))
