@@ -131,6 +131,7 @@ _SIGNATURES = {
     "dpp_launch_count": (ctypes.c_uint64, []),
     "dpp_set_attn_core_events": (None, [_vp, _vp]),
     "dpp_workspace_bytes": (_sz, [ctypes.c_int, _vp]),
+    "dpp_wait_selftest": (_st, [ctypes.c_int, _vp, _vp]),
     "dpp_layernorm": (_st, [ctypes.POINTER(dpp_ln_desc), _vp, _vp, _vp, _vp, _vp]),
     "dpp_linear": (_st, [ctypes.POINTER(dpp_linear_desc), _vp, _vp, _vp, _vp, _vp]),
     "dpp_switch_init": (None, [ctypes.POINTER(dpp_switch_state), ctypes.c_double,
@@ -223,6 +224,11 @@ def dpp_groupnorm_apply(desc: dpp_gn_desc, x, stats_prev, gn_sums, stats_next, g
                                           _ptr(gn_sums), _ptr(stats_next), _ptr(gamma),
                                           _ptr(beta), _ptr(y), _stream(stream)),
                   "dpp_groupnorm_apply", raise_on_error)
+
+
+def dpp_wait_selftest(kind: int, scratch=None, stream=None, raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_wait_selftest(int(kind), _ptr(scratch), _stream(stream)),
+                  "dpp_wait_selftest", raise_on_error)
 
 
 def dpp_workspace_bytes(op: int, desc) -> int:

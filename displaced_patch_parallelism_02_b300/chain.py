@@ -56,9 +56,19 @@ def weight_shapes(C, F, c_ctx):
     return shapes
 
 
+def full_device(device):
+    """torch.device with its index filled in ("cuda" -> "cuda:<current>"),
+    so that it compares equal to a tensor's device."""
+    dev = torch.device(device)
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    return dev
+
+
 def check_weights(weights, C, F, c_ctx, dev):
     """The library reads weights through raw pointers, so their shapes,
     types, device and layout are checked here once, on the host."""
+    dev = full_device(dev)
     shapes = weight_shapes(C, F, c_ctx)
     missing = [k for k in shapes if k not in weights]
     if missing:
@@ -83,7 +93,7 @@ class BlockChain:
                  ff_mult=4, eps_gn_res=1e-5, eps_gn_tf=1e-6, eps_ln=1e-5):
         self.B, self.H, self.W, self.C, self.P, self.G = B, H, W, C, P, G
         self.heads, self.n_ctx, self.c_ctx, self.F = heads, n_ctx, c_ctx, ff_mult * C
-        dev = torch.device(device)
+        dev = full_device(device)
         self.w = check_weights(weights, C, self.F, c_ctx, dev)
         bf = torch.bfloat16
         N, M = H * W, B * H * W
@@ -214,7 +224,7 @@ class BranchPair:
     of a branch does not depend on the schedule."""
 
     def __init__(self, H, W, C, heads, P, G, n_ctx, c_ctx, weights, device, **kw):
-        dev = torch.device(device)
+        dev = full_device(device)
         self.branches = [BlockChain(1, H, W, C, heads, P, G, n_ctx, c_ctx, weights, dev, **kw)
                          for _ in range(2)]
         self.side = torch.cuda.Stream(dev)

@@ -435,6 +435,17 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
                             (int)nt, s));
 }
 
+dpp_status dpp_wait_selftest(int kind, void *scratch, dpp_stream stream) {
+  if (kind != 0 && kind != 1) return DPP_ERR_INVALID_ARG;
+  if (kind == 0 && !scratch) return DPP_ERR_INVALID_ARG;
+  if (scratch && !aligned16(scratch)) return DPP_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (kind == 0)
+    return from_cuda(counted(
+        launch_wait_selftest_counter(reinterpret_cast<const unsigned *>(scratch), s), 1));
+  return from_cuda(counted(launch_wait_selftest_mbarrier(s), 1));
+}
+
 size_t dpp_workspace_bytes(int op, const void *desc) {
   if (!desc) return 0;
   switch (op) {

@@ -124,6 +124,10 @@ bool attn_tc_supported(const AttnArgs &a);
 cudaError_t launch_layernorm(const dpp_ln_desc &d, const void *x, const float *gamma,
                              const float *beta, void *y, cudaStream_t s);
 
+// self-tests of the two bounded waits (see dpp_wait_selftest)
+cudaError_t launch_wait_selftest_counter(const unsigned *counter, cudaStream_t s);
+cudaError_t launch_wait_selftest_mbarrier(cudaStream_t s);
+
 // device status word (bounded waits record DPP_ERR_TIMEOUT here)
 int *device_status_ptr();
 

@@ -411,6 +411,30 @@ __global__ void cast_bf16_f16_kernel(const __nv_bfloat16 *__restrict__ in, __hal
 
 }  // namespace
 
+namespace {
+
+// Self-test of the bounded mbarrier wait every tensor-core kernel uses: one
+// thread waits for the first phase of a barrier nobody arrives on; after the
+// wait limit mbar_wait records DPP_ERR_TIMEOUT and returns false.
+__global__ void mbar_wait_selftest_kernel(int *status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0u, &abort_flag, status);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest_mbarrier(cudaStream_t s) {
+  mbar_wait_selftest_kernel<<<1, 32, 0, s>>>(device_status_ptr());
+  return cudaGetLastError();
+}
+
 cudaError_t launch_cast_bf16_f16(const void *in, void *out, size_t n, cudaStream_t s) {
   size_t blocks = (n + 255) / 256;
   if (blocks > 1184) blocks = 1184;

@@ -573,7 +573,20 @@ cudaError_t run_gn(const dpp_gn_desc &d, const void *x, const float *stats_prev,
                                      smem, s);
 }
 
+// Self-test of the bounded wait above: one thread waits for a unit counter
+// that nothing advances; after the wait limit it records DPP_ERR_TIMEOUT in
+// the status word and the kernel returns.
+__global__ void gn_wait_selftest_kernel(const unsigned *counter, int *status) {
+  __shared__ int flag;
+  gn_wait_units(counter, 0, 0, 1u, &flag, status);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest_counter(const unsigned *counter, cudaStream_t s) {
+  gn_wait_selftest_kernel<<<1, 32, 0, s>>>(counter, device_status_ptr());
+  return cudaGetLastError();
+}
 
 size_t gn_workspace(const dpp_gn_desc &d) { return gn_layout(d, nullptr, nullptr); }
 

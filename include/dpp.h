@@ -354,6 +354,20 @@ dpp_status dpp_linear(const dpp_linear_desc *desc, const void *x, const void *w,
                       const float *bias, void *y, dpp_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * dpp_wait_selftest -- exercises one of the library's bounded device waits
+ * against an event that never comes, so that failure detection can be
+ * tested without a fault: the kernel waits its limit (1 s), records
+ * DPP_ERR_TIMEOUT in the status word (read it with dpp_device_status) and
+ * returns; the context stays usable.
+ *   kind 0: the acquire-poll wait on a unit counter (the cooperative
+ *           GroupNorm's); scratch = 16 bytes of device memory holding zeros,
+ *           which nothing advances.
+ *   kind 1: the mbarrier wait of the tensor-core kernels; scratch unused.
+ * Returns DPP_OK once the kernel is launched; it runs for about a second.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_wait_selftest(int kind, void *scratch, dpp_stream stream);
+
+/* ---------------------------------------------------------------------------
  * dpp_workspace_bytes -- the workspace any entry point needs, by op: the
  * per-op queries above behind one call.  desc points to the op's descriptor
  * (dpp_gn_desc for DPP_OP_GROUPNORM, dpp_attn_desc for the attention ops,

@@ -289,3 +289,12 @@ def test_block_chain_checks_weight_shapes_on_the_host():
     bad = dict(w, conv1_w=torch.zeros((C, C, 3, 3), dtype=torch.bfloat16))  # not channels-last
     with pytest.raises(ValueError, match="conv1_w"):
         chain.check_weights(bad, C, F, X, torch.device("cpu"))
+
+
+def test_wait_selftest_validation():
+    before = dpp.dpp_launch_count()
+    assert dpp.dpp_wait_selftest(2, A, stream=0, raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+    assert dpp.dpp_wait_selftest(0, None, stream=0, raise_on_error=False) == \
+        dpp.DPP_ERR_INVALID_ARG
+    assert dpp.dpp_wait_selftest(0, A + 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_ALIGN
+    assert dpp.dpp_launch_count() == before
