@@ -94,6 +94,7 @@ class BlockChain:
         self.B, self.H, self.W, self.C, self.P, self.G = B, H, W, C, P, G
         self.heads, self.n_ctx, self.c_ctx, self.F = heads, n_ctx, c_ctx, ff_mult * C
         dev = full_device(device)
+        self.dev = dev
         self.w = check_weights(weights, C, self.F, c_ctx, dev)
         bf = torch.bfloat16
         N, M = H * W, B * H * W
@@ -148,6 +149,12 @@ class BlockChain:
         the text context ctx ([B, n_ctx, c_ctx] bf16).  hook(op, when, tensors),
         when given, is called before ("pre") and after ("post") every op with
         the op's input and output tensors (for tests that check op by op)."""
+        for name, t, shape in (("x", x, (self.B, self.H, self.W, self.C)),
+                               ("ctx", ctx, (self.B, self.n_ctx, self.c_ctx))):
+            if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or \
+                    not t.is_contiguous() or t.device != self.dev:
+                raise ValueError(f"{name}: want {shape} bf16 contiguous on {self.dev}, got "
+                                 f"{tuple(t.shape)} {t.dtype} on {t.device}")
         w, s = self.w, stream
         i, j = self.k % 2, 1 - self.k % 2
         first = self.k == 0

@@ -298,3 +298,24 @@ def test_wait_selftest_validation():
         dpp.DPP_ERR_INVALID_ARG
     assert dpp.dpp_wait_selftest(0, A + 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_ALIGN
     assert dpp.dpp_launch_count() == before
+
+
+def test_block_chain_step_checks_its_inputs_on_the_host():
+    import torch
+    from displaced_patch_parallelism_02_b300 import chain
+    C, F, X = 64, 256, 32
+    w = {k: torch.zeros(s, dtype=torch.float32 if len(s) == 1 else torch.bfloat16)
+         for k, s in chain.weight_shapes(C, F, X).items()}
+    bc = chain.BlockChain(1, 8, 8, C, 1, 2, 8, 5, X, w, "cpu")
+    x = torch.zeros(1, 8, 8, C, dtype=torch.bfloat16)
+    ctx = torch.zeros(1, 5, X, dtype=torch.bfloat16)
+    n0 = dpp.dpp_launch_count()
+    with pytest.raises(ValueError, match="x:"):
+        bc.step(torch.zeros(1, 8, 4, C, dtype=torch.bfloat16), ctx)
+    with pytest.raises(ValueError, match="x:"):
+        bc.step(x.float(), ctx)
+    with pytest.raises(ValueError, match="ctx:"):
+        bc.step(x, torch.zeros(1, 5, 16, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="x:"):
+        bc.step(torch.zeros(1, 8, 8, 2 * C, dtype=torch.bfloat16)[..., :C], ctx)  # strided
+    assert dpp.dpp_launch_count() == n0 and bc.k == 0
