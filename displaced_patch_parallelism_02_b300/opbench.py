@@ -1,0 +1,121 @@
+"""Times one library call at a given shape: the single-kernel view that
+profiling needs (ncu -k ... -s <warm-up launches> -c ...).
+
+    python -m displaced_patch_parallelism_02_b300.opbench linear --M 65536 --K 2560 --N 640 \
+        --bias --accumulate
+    python -m displaced_patch_parallelism_02_b300.opbench cfg --n 921600
+    python -m displaced_patch_parallelism_02_b300.opbench conv_gn --H 512 --W 512 --C 320 --P 8
+    python -m displaced_patch_parallelism_02_b300.opbench layernorm --T 262144 --C 640
+
+Inputs are seeded random device tensors (bf16 activations, weights scaled by
+1/sqrt(fan_in), fp32 guidance maps); `--warmup` calls run first, then `--reps`
+calls between two CUDA events.  Prints one JSON line with the time per call
+and the achieved TFLOP/s (contractions) or GB/s (read x + write y).
+Every call is the library's own entry point; nothing here computes anything.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import (DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_cfg_combine, dpp_cfg_workspace_bytes,
+               dpp_conv3x3_gn, dpp_conv_desc, dpp_device_status, dpp_gn_desc,
+               dpp_groupnorm_apply, dpp_layernorm, dpp_linear, dpp_linear_desc, dpp_ln_desc)
+
+
+def _randn(shape, gen, scale=1.0, dtype=torch.bfloat16):
+    return (torch.randn(shape, generator=gen, device="cuda") * scale).to(dtype)
+
+
+def setup(args, gen):
+    """Returns (call, work, unit) for the op: call() makes one library call,
+    work is the FLOPs or bytes of one call."""
+    if args.op == "linear":
+        M, K, N = args.M, args.K, args.N
+        rows = 2 * N if args.geglu else N
+        x = _randn((M, K), gen)
+        w = _randn((rows, K), gen, K ** -0.5)
+        b = _randn((rows,), gen, 0.1, torch.float32) if args.bias else None
+        y = _randn((M, N), gen)
+        d = dpp_linear_desc(M, K, N, DPP_BF16, DPP_EPI_GEGLU if args.geglu else DPP_EPI_NONE,
+                            int(args.accumulate))
+        return (lambda: dpp_linear(d, x, w, b, y)), 2.0 * M * K * rows, "TFLOP/s"
+    if args.op == "cfg":
+        n = args.n
+        u, c = _randn((n,), gen, dtype=torch.float32), _randn((n,), gen, dtype=torch.float32)
+        out = torch.empty_like(u)
+        sums = torch.zeros(3, dtype=torch.float64, device="cuda")
+        nws = dpp_cfg_workspace_bytes(n)
+        ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+        return (lambda: dpp_cfg_combine(u, c, 7.5, n, out, sums, ws, nws)), 12.0 * n, "GB/s"
+    if args.op == "conv_gn":
+        B, H, W, C, P, G = args.B, args.H, args.W, args.C, args.P, args.G
+        x = _randn((B, H, W, C), gen)
+        stale = _randn((B, H, W, C), gen)
+        w = _randn((C, 3, 3, C), gen, (9 * C) ** -0.5)
+        y, y2 = torch.empty_like(x), torch.empty_like(x)
+        sums = torch.empty((P, B, G, 2), dtype=torch.float64, device="cuda")
+        st_prev = torch.zeros((P, B, G, 2), device="cuda")
+        st_next = torch.empty_like(st_prev)
+        gamma, beta = torch.ones(C, device="cuda"), torch.zeros(C, device="cuda")
+        cd = dpp_conv_desc(B, H, W, C, C, P, DPP_BF16, 0, 0)
+        gd = dpp_gn_desc(B, H, W, C, G, P, 1e-5, DPP_BF16, 0, 0)
+
+        def call():
+            dpp_conv3x3_gn(cd, x, stale, w, None, y, G, sums)
+            dpp_groupnorm_apply(gd, y, st_prev, sums, st_next, gamma, beta, y2)
+        return call, 2.0 * B * H * W * C * 9 * C, "TFLOP/s"
+    if args.op == "layernorm":
+        T, C = args.T, args.C
+        x = _randn((T, C), gen)
+        y = torch.empty_like(x)
+        g, b = torch.ones(C, device="cuda"), torch.zeros(C, device="cuda")
+        d = dpp_ln_desc(T, C, 1e-5, DPP_BF16)
+        return (lambda: dpp_layernorm(d, x, g, b, y)), 2.0 * 2 * T * C, "GB/s"
+    raise ValueError(args.op)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm"])
+    ap.add_argument("--M", type=int, default=115200)
+    ap.add_argument("--K", type=int, default=640)
+    ap.add_argument("--N", type=int, default=640)
+    ap.add_argument("--bias", action="store_true")
+    ap.add_argument("--accumulate", action="store_true")
+    ap.add_argument("--geglu", action="store_true")
+    ap.add_argument("--n", type=int, default=4 * 480 * 480)
+    ap.add_argument("--B", type=int, default=1)
+    ap.add_argument("--H", type=int, default=512)
+    ap.add_argument("--W", type=int, default=512)
+    ap.add_argument("--C", type=int, default=320)
+    ap.add_argument("--P", type=int, default=8)
+    ap.add_argument("--G", type=int, default=32)
+    ap.add_argument("--T", type=int, default=262144)
+    ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--reps", type=int, default=1)
+    args = ap.parse_args(argv)
+    assert torch.cuda.is_available(), "opbench needs a CUDA device"
+    gen = torch.Generator(device="cuda").manual_seed(1234)
+    call, work, unit = setup(args, gen)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.reps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / max(args.reps, 1)
+    rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    out = {k: v for k, v in vars(args).items()}
+    out.update(ms_per_call=ms, achieved=rate, unit=unit, status=dpp_device_status())
+    print(json.dumps(out))
+    return 0 if out["status"] == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
