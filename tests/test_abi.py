@@ -319,3 +319,16 @@ def test_block_chain_step_checks_its_inputs_on_the_host():
     with pytest.raises(ValueError, match="x:"):
         bc.step(torch.zeros(1, 8, 8, 2 * C, dtype=torch.bfloat16)[..., :C], ctx)  # strided
     assert dpp.dpp_launch_count() == n0 and bc.k == 0
+
+
+def test_opbench_parses_its_options_and_needs_a_device():
+    import torch
+    from displaced_patch_parallelism_02_b300 import opbench
+    with pytest.raises(SystemExit) as e:
+        opbench.main(["--help"])
+    assert e.value.code == 0
+    with pytest.raises(SystemExit):
+        opbench.main(["no_such_op"])
+    if not torch.cuda.is_available():
+        with pytest.raises(AssertionError, match="CUDA device"):
+            opbench.main(["linear", "--M", "128"])
