@@ -6,7 +6,7 @@
 // O = softmax(Q K^T / 8) V per (batch, head, band), head_dim 64, fp16 Q/K/V/P,
 // fp32 accumulators and softmax.  One CTA handles two 128-query tiles of one
 // band so that one tile's softmax overlaps the other tile's MMAs:
-//   warp 0        TMA producer: both Q tiles once, then K and V tiles of 128
+//   warp 0        TMA producer (converged warp, elected lane): both Q tiles once, then K and V tiles of 128
 //                 keys into 4-deep rings (128-byte swizzle).  The key range is
 //                 walked segment by segment -- own band from the fresh state,
 //                 the keys before and after it from the stale state -- so each
@@ -14,22 +14,28 @@
 //                 to end at the segment end (masking its leading columns), so
 //                 no tile reads outside its segment when the segment holds at
 //                 least 128 keys.
-//   warps 1, 10   one MMA-issuing thread per query tile t (warp 1 also owns
-//                 the TMEM allocation):
+//   warps 1, 2    one MMA-issuing warp per query tile t (warp 1 also owns
+//                 the TMEM allocation); the warp stays converged and one
+//                 elected lane issues each MMA:
 //                   S_t = Q_t K^T   (M 128, N 128, K 64), both from shared memory,
 //                   O_t += P_t V    (M 128, N 64, K 128), P_t read from tensor
 //                                   memory, V from shared memory (MN-major);
 //                 separate issuers keep one tile's wait for its softmax from
 //                 stalling the other tile's MMAs.
-//   warps 2..5    softmax of query tile 0, warps 6..9 of tile 1: one thread
-//                 per query row (= TMEM lane); row max (3-input max, four
-//                 independent chains), p = 2^(s*scale - m) with the scale
-//                 folded into paired fp32 FMAs and the exponentials on the
-//                 special-function unit, running sum in paired fp32 adds, P
-//                 written back to tensor memory as fp16 pairs; the reference
-//                 max m only moves when a row max exceeds it by 8 (in log2
-//                 units), so the O accumulator in TMEM is rarely rescaled;
-//                 final O / l stored as fp16.
+//   warps 3..18   softmax, eight warps per query tile, two threads per query
+//                 row: a warp reads 16 TMEM lanes (rows) with the 16x32bx2
+//                 access shape, its lanes 0..15 taking keys 0..63 of a row
+//                 and lanes 16..31 keys 64..127, so every scheduler runs four
+//                 softmax warps.  The two halves of a row agree on its max
+//                 with one shuffle; each keeps its own partial row sum.  Row
+//                 max (3-input max, four independent chains), p = 2^(s*scale
+//                 - m) with the scale folded into paired fp32 FMAs and the
+//                 exponentials taken as fp16 pairs on the special-function
+//                 unit (P's fp16 pairs come out directly), running sum in
+//                 paired fp16 adds folded into fp32 per tile, P written back
+//                 to tensor memory; the reference max m only moves when a row
+//                 max exceeds it by 4 (in log2 units), so the O accumulator in
+//                 TMEM is rarely rescaled; final O / l stored as fp16.
 //
 // Tensor memory per query tile t (256 columns at t * 256): S in columns
 // [0, 128), O in [128, 192), P in [192, 256) (fp16 pairs).  Keeping P out of
@@ -43,7 +49,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 352;  // 11 warps
+constexpr int kThreads = 608;  // 19 warps: producer, two MMA issuers, 16 softmax
 constexpr int KS = 4, VS = 4;  // K and V ring depths
 constexpr uint32_t TILE_BYTES = 128 * 128;  // 128 rows x 64 fp16
 constexpr uint32_t OFF_Q = 0;
@@ -51,7 +57,7 @@ constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
-constexpr float kRescaleThreshold = 8.f;
+constexpr float kRescaleThreshold = 4.f;
 
 struct AttnTcParams {
   int B, Nq, Nkv, C, P;
@@ -119,35 +125,69 @@ __device__ __forceinline__ KvTile tile_of(const Segs &s, int j) {
   return t;
 }
 
-// ---- paired fp32 arithmetic (sm_100 family) and the exponential
+// 2^x for an fp16 pair on the special-function unit
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// ---- 3-input max (sm_100 family)
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
-__device__ __forceinline__ uint64_t f2pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t v, float &a, float &b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
+// ---- grouped MMA issue: one asm block, one elected lane, the whole group.
+// S = Q K^T over K = 64 (four K16 steps; descriptors advance 32 bytes per
+// step inside the 128-byte swizzled rows), then the two commits.
+__device__ __forceinline__ void issue_s(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                        uint64_t *done, uint64_t *slot_free) {
+  asm volatile(
+      "{\n\t.reg .pred e, pf, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, pt;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(smem_u32(done)), "r"(smem_u32(slot_free))
+      : "memory");
 }
 
-__device__ __forceinline__ uint64_t exp2_mufu2(uint64_t x2) {
-  float a, b;
-  f2unpack(x2, a, b);
-  return f2pack(ex2_approx(a), ex2_approx(b));
+// O (+)= P V over K = 128 keys: eight K16 steps, P from tensor memory (8
+// columns of fp16 pairs per step), V from shared memory MN-major (16 rows of
+// 128 bytes = 2048 bytes, i.e. 128 descriptor units, per step); `first`
+// starts the accumulator instead of adding to it.  Then the two commits.
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t bd, uint32_t idesc,
+                                         uint32_t first, uint64_t *done, uint64_t *slot_free) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, pt;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+      "setp.eq.b32 p0, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "add.s32 a1, %1, 8;\n\tadd.s32 a2, %1, 16;\n\tadd.s32 a3, %1, 24;\n\t"
+      "add.s32 a4, %1, 32;\n\tadd.s32 a5, %1, 40;\n\tadd.s32 a6, %1, 48;\n\t"
+      "add.s32 a7, %1, 56;\n\t"
+      "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+      "add.s64 b4, %2, 512;\n\tadd.s64 b5, %2, 640;\n\tadd.s64 b6, %2, 768;\n\t"
+      "add.s64 b7, %2, 896;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, pt;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, pt;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}" ::"r"(d),
+      "r"(a), "l"(bd), "r"(idesc), "r"(first), "r"(smem_u32(done)), "r"(smem_u32(slot_free))
+      : "memory");
 }
 
 // Warp-uniform bounded wait: every lane waits, then the warp agrees.
@@ -189,8 +229,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 2); }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&s_empty[t], 4);  // one arrival per softmax warp
-      mbar_init(&p_full[t], 4);
+      mbar_init(&s_empty[t], 8);  // one arrival per softmax warp of the tile
+      mbar_init(&p_full[t], 8);
       mbar_init(&p_empty[t], 1);
       mbar_init(&o_final[t], 1);
       mbar_init(&drain[t], 1);
@@ -212,158 +252,157 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {  // ------------------------------------------ producer
-      uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
-      mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
-      tma_load_2d(smem + OFF_Q, &tmQ, q_full, head * 64, b * p.Nq + q0);
-      tma_load_2d(smem + OFF_Q + TILE_BYTES, &tmQ, q_full, head * 64, b * p.Nq + q0 + 128);
-      for (int j = 0; j < T; ++j) {
-        const KvTile kt = tile_of(segs, j);
-        const CUtensorMap *m = kt.fresh ? &tmF : &tmS;
-        const int row = b * p.Nkv + kt.kv0;
-        const int ks = j % KS, vs = j % VS;
-        const uint32_t kph = (j / KS) & 1, vph = (j / VS) & 1;
-        if (!mbar_wait(&k_empty[ks], kph ^ 1u, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&k_full[ks], TILE_BYTES);
-        k_armed |= 1u << ks;
-        k_par = (k_par & ~(1u << ks)) | (kph << ks);
-        tma_load_2d(smem + OFF_K + ks * TILE_BYTES, m, &k_full[ks], head * 64, row);
-        if (!mbar_wait(&v_empty[vs], vph ^ 1u, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&v_full[vs], TILE_BYTES);
-        v_armed |= 1u << vs;
-        v_par = (v_par & ~(1u << vs)) | (vph << vs);
-        tma_load_2d(smem + OFF_V + vs * TILE_BYTES, m, &v_full[vs], p.C + head * 64, row);
-      }
-      if (*abort_flag) {  // copies in flight must land before the CTA exits
-        mbar_drain(q_full, 0);
-        for (int i = 0; i < KS; ++i)
-          if ((k_armed >> i) & 1u) mbar_drain(&k_full[i], (k_par >> i) & 1u);
-        for (int i = 0; i < VS; ++i)
-          if ((v_armed >> i) & 1u) mbar_drain(&v_full[i], (v_par >> i) & 1u);
-      }
+  if (warp == 0) {  // ------------------------------------------------ producer
+    // The whole warp runs the loop (warp-uniform operands); one elected lane
+    // issues each copy.
+    uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
+    mbar_arrive_expect_tx_w(q_full, 2 * TILE_BYTES);
+    tma_load_2d_w(smem + OFF_Q, &tmQ, q_full, head * 64, b * p.Nq + q0);
+    tma_load_2d_w(smem + OFF_Q + TILE_BYTES, &tmQ, q_full, head * 64, b * p.Nq + q0 + 128);
+    for (int j = 0; j < T; ++j) {
+      const KvTile kt = tile_of(segs, j);
+      const CUtensorMap *m = kt.fresh ? &tmF : &tmS;
+      const int row = b * p.Nkv + kt.kv0;
+      const int ks = j % KS, vs = j % VS;
+      const uint32_t kph = (j / KS) & 1, vph = (j / VS) & 1;
+      if (!mbar_wait_w(&k_empty[ks], kph ^ 1u, abort_flag, p.status)) break;
+      mbar_arrive_expect_tx_w(&k_full[ks], TILE_BYTES);
+      k_armed |= 1u << ks;
+      k_par = (k_par & ~(1u << ks)) | (kph << ks);
+      tma_load_2d_w(smem + OFF_K + ks * TILE_BYTES, m, &k_full[ks], head * 64, row);
+      if (!mbar_wait_w(&v_empty[vs], vph ^ 1u, abort_flag, p.status)) break;
+      mbar_arrive_expect_tx_w(&v_full[vs], TILE_BYTES);
+      v_armed |= 1u << vs;
+      v_par = (v_par & ~(1u << vs)) | (vph << vs);
+      tma_load_2d_w(smem + OFF_V + vs * TILE_BYTES, m, &v_full[vs], p.C + head * 64, row);
     }
-  } else if (warp == 1 || warp == 10) {
-    if (lane == 0) {  // ------------------------- MMA issuer of query tile t
-      // Each query tile has its own issuing thread, so one tile's wait for
-      // its softmax never holds back the other tile's MMAs.  Per key tile j:
-      // S(j) = Q K(j)^T as soon as the softmax has read S(j-1), then
-      // O += P(j-1) V(j-1) once it has written P(j-1).
-      const int t = warp == 1 ? 0 : 1;
-      constexpr uint32_t IDESC_S = idesc_f16(128, 128, false);
-      constexpr uint32_t IDESC_O = idesc_f16(128, 64, false, true);
-      const uint32_t sQ = smem_u32(smem + OFF_Q) + t * TILE_BYTES, sK = smem_u32(smem + OFF_K);
-      const uint32_t sV = smem_u32(smem + OFF_V);
-      const uint32_t dS = tmem + t * 256, dO = dS + 128, aP = dS + 192;
-      auto pv = [&](int j) -> bool {  // O += P(j) V(j)
-        if (!mbar_wait(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status)) return false;
-        if (!mbar_wait(&p_full[t], j & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint32_t vb = sV + (j % VS) * TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // 16 keys: 8 TMEM columns of P, 16 rows of V
-          mma_f16_ts(dO, aP + kk * 8, desc_sw128_mnmajor(vb + kk * 2048, 1024), IDESC_O,
-                     (j | kk) != 0);
-        mma_commit(&p_empty[t]);
-        mma_commit(&v_empty[j % VS]);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      const uint64_t ad = desc_sw128_kmajor(sQ);
-      for (int j = 0; ok && j < T; ++j) {
-        ok = mbar_wait(&k_full[j % KS], (j / KS) & 1, abort_flag, p.status) &&
-             mbar_wait(&s_empty[t], (j & 1) ^ 1u, abort_flag, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t bd = desc_sw128_kmajor(sK + (j % KS) * TILE_BYTES);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mma_f16_ss(dS, ad + 2 * k, bd + 2 * k, IDESC_S, k);
-        mma_commit(&s_full[t]);
-        mma_commit(&k_empty[j % KS]);
-        if (j > 0) ok = pv(j - 1);
-      }
-      if (ok && T > 0) ok = pv(T - 1);
-      if (ok) {
-        mma_commit(&o_final[t]);
-      } else {  // nothing may still be writing TMEM when it is freed
-        mma_commit(&drain[t]);
-        mbar_drain(&drain[t], 0);
-      }
+    if (*abort_flag) {  // copies in flight must land before the CTA exits
+      mbar_drain(q_full, 0);
+      for (int i = 0; i < KS; ++i)
+        if ((k_armed >> i) & 1u) mbar_drain(&k_full[i], (k_par >> i) & 1u);
+      for (int i = 0; i < VS; ++i)
+        if ((v_armed >> i) & 1u) mbar_drain(&v_full[i], (v_par >> i) & 1u);
+    }
+  } else if (warp == 1 || warp == 2) {  // ------------- MMA issuer of query tile t
+    // Each query tile has its own issuing warp, so one tile's wait for its
+    // softmax never holds back the other tile's MMAs.  Per key tile j:
+    // S(j) = Q K(j)^T as soon as the softmax has read S(j-1), then
+    // O += P(j-1) V(j-1) once it has written P(j-1).  The warp stays
+    // converged; one elected lane issues each MMA and commit.
+    const int t = warp - 1;
+    constexpr uint32_t IDESC_S = idesc_f16(128, 128, false);
+    constexpr uint32_t IDESC_O = idesc_f16(128, 64, false, true);
+    const uint32_t sQ = smem_u32(smem + OFF_Q) + t * TILE_BYTES, sK = smem_u32(smem + OFF_K);
+    const uint32_t sV = smem_u32(smem + OFF_V);
+    const uint32_t dS = tmem + t * 256, dO = dS + 128, aP = dS + 192;
+    auto pv = [&](int j) -> bool {  // O += P(j) V(j)
+      if (!mbar_wait_w(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status)) return false;
+      if (!mbar_wait_w(&p_full[t], j & 1, abort_flag, p.status)) return false;
+      tc_fence_after();
+      issue_pv(dO, aP, desc_sw128_mnmajor(sV + (j % VS) * TILE_BYTES, 1024), IDESC_O,
+               j == 0 ? 1u : 0u, &p_empty[t], &v_empty[j % VS]);
+      return true;
+    };
+    bool ok = mbar_wait_w(q_full, 0, abort_flag, p.status);
+    const uint64_t ad = desc_sw128_kmajor(sQ);
+    for (int j = 0; ok && j < T; ++j) {
+      ok = mbar_wait_w(&k_full[j % KS], (j / KS) & 1, abort_flag, p.status) &&
+           mbar_wait_w(&s_empty[t], (j & 1) ^ 1u, abort_flag, p.status);
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(dS, ad, desc_sw128_kmajor(sK + (j % KS) * TILE_BYTES), IDESC_S, &s_full[t],
+              &k_empty[j % KS]);
+      if (j > 0) ok = pv(j - 1);
+    }
+    if (ok && T > 0) ok = pv(T - 1);
+    if (ok) {
+      mma_commit_w(&o_final[t]);
+    } else {  // nothing may still be writing TMEM when it is freed
+      mma_commit_w(&drain[t]);
+      mbar_drain(&drain[t], 0);
     }
   } else {  // ------------------------------------------------------ softmax
-    const int t = (warp - 2) / 4;
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int sw = warp - 3;                // 0..15
+    const int t = sw >> 3;                  // query tile
+    const int quad = warp & 3;              // TMEM lanes this warp may access: 32*quad..
+    const int h16 = (sw >> 2) & 1;          // which 16 of them
+    const int half = lane >> 4;             // keys [64*half, 64*half + 64) of each tile
+    const int row = quad * 32 + h16 * 16 + (lane & 15);
+    const uint32_t lane_base = (uint32_t)(quad * 32 + h16 * 16) << 16;
     const uint32_t tS = tmem + lane_base + t * 256, tO = tS + 128, tP = tS + 192;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;  // l: this thread's half of the row sum
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const KvTile kt = tile_of(segs, j);
       if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t (&r)[32] = *reinterpret_cast<uint32_t (*)[32]>(&sr[32 * c]);
-        tmem_ld32(tS + 32 * c, r);
-      }
+      uint32_t sr[64];
+      tmem_ld16x2_32<64>(tS, *reinterpret_cast<uint32_t (*)[32]>(&sr[0]));
+      tmem_ld16x2_32<64>(tS + 32, *reinterpret_cast<uint32_t (*)[32]>(&sr[32]));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[t]);
       if (kt.vlo != 0 || kt.vhi != 128) {  // ragged tile (uniform branch): mask
+        const int k0 = half * 64;
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i < kt.vlo || i >= kt.vhi) sr[i] = 0xff800000u;  // -inf
+        for (int i = 0; i < 64; ++i)
+          if (k0 + i < kt.vlo || k0 + i >= kt.vhi) sr[i] = 0xff800000u;  // -inf
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 128; i += 8)
+      for (int i = 0; i < 64; i += 8)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           m4[k] = max3f(m4[k], __uint_as_float(sr[i + 2 * k]), __uint_as_float(sr[i + 2 * k + 1]));
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+      float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));  // the row's other half
+      const float mx = mh * p.scale_log2;
       float corr = 1.f;
-      if (mx > m_ref + kRescaleThreshold) {
+      if (mx > m_ref + kRescaleThreshold) {  // both halves of the row decide alike
         corr = ex2_approx(m_ref - mx);  // 0 on the first tile
         m_ref = mx;
       }
       l *= corr;
-      // p = 2^(s * scale - m_ref), packed as fp16 pairs into pk[0..63]
-      const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_ref, -m_ref);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[64];
+      // p = 2^(s * scale - m_ref): the scaled argument of each pair of scores
+      // (paired fp32 FMA) is rounded to an fp16 pair and exponentiated on the
+      // special-function unit as a pair (ex2.approx.f16x2), which yields P's
+      // fp16 pairs directly: two exponentials per instruction.  With m_ref at
+      // most kRescaleThreshold below the running max, every argument is <= 4,
+      // where fp16 resolves it to 2^-9 (p within 0.07 %).  The half-row sum
+      // is taken over the fp16 pairs (four chains of paired fp16 adds, each
+      // pair's sum at most 64 x 16) and added to l in fp32.
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nm2 = make_float2(-m_ref, -m_ref);
+      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const uint64_t x2 =
-            ffma2(f2pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sc2, nm2);
-        const uint64_t e2 = exp2_mufu2(x2);
-        acc2[i & 3] = fadd2(acc2[i & 3], e2);
-        float a, bb;
-        f2unpack(e2, a, bb);
-        pk[i] = pack_half2(a, bb);
+      for (int i = 0; i < 32; ++i) {
+        const float2 x = __ffma2_rn(
+            make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sc2, nm2);
+        pk[i] = ex2_f16x2(pack_half2(x.x, x.y));
       }
+      __half2 acc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] = *reinterpret_cast<const __half2 *>(&pk[k]);
+#pragma unroll
+      for (int i = 4; i < 32; ++i)
+        acc[i & 3] = __hadd2(acc[i & 3], *reinterpret_cast<const __half2 *>(&pk[i]));
       {
-        float a, bb;
-        f2unpack(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), a, bb);
-        l += a + bb;
+        const float2 a0 = __half22float2(acc[0]), a1 = __half22float2(acc[1]);
+        const float2 a2 = __half22float2(acc[2]), a3 = __half22float2(acc[3]);
+        l += ((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y));
       }
       // PV(j-1) must be done reading P and writing O before both are rewritten
       if (!warp_wait(&p_empty[t], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      tmem_st32(tP, *reinterpret_cast<uint32_t (*)[32]>(&pk[0]));
-      tmem_st32(tP + 32, *reinterpret_cast<uint32_t (*)[32]>(&pk[32]));
+      tmem_st16x2_32<32>(tP, pk);  // lanes 0..15: P columns 0..31, lanes 16..31: 32..63
       if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // rescale O (rare)
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + 32 * c, r);
-          tmem_wait_ld();
+        uint32_t r[32];
+        tmem_ld16x2_32<32>(tO, r);  // each half of the row rescales 32 of its 64 columns
+        tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-          tmem_st32(tO + 32 * c, r);
-        }
+        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+        tmem_st16x2_32<32>(tO, r);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -373,25 +412,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if (ok && warp_wait(&o_final[t], 0, abort_flag, p.status)) {
       tc_fence_after();
       const int q = q0 + t * 128 + row;
-      const float inv = 1.f / l;
+      const float inv = 1.f / (l + __shfl_xor_sync(0xffffffffu, l, 16));
+      uint32_t r[32];
+      tmem_ld16x2_32<32>(tO, r);  // lanes 0..15: O columns 0..31, lanes 16..31: 32..63
+      tmem_wait_ld();
+      if (q < qend) {
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(p.o) +
+                                               ((size_t)b * p.Nq + q) * p.C + head * 64 +
+                                               32 * half);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tO + 32 * c, r);
-        tmem_wait_ld();
-        if (q < qend) {
-          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(p.o) +
-                                                 ((size_t)b * p.Nq + q) * p.C + head * 64 + 32 * c);
+        for (int v = 0; v < 4; ++v) {
+          uint4 o;
+          uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              ow[e] = pack_half2(__uint_as_float(r[8 * v + 2 * e]) * inv,
-                                 __uint_as_float(r[8 * v + 2 * e + 1]) * inv);
-            dst[v] = o;
-          }
+          for (int e = 0; e < 4; ++e)
+            ow[e] = pack_half2(__uint_as_float(r[8 * v + 2 * e]) * inv,
+                               __uint_as_float(r[8 * v + 2 * e + 1]) * inv);
+          dst[v] = o;
         }
       }
     }

@@ -12,10 +12,12 @@
 // and TMA fills them with zeros: the image padding costs nothing.
 //
 // Persistent, warp-specialised, one CTA per SM (the GEMM kernel's layout):
-//   warp 0      TMA producer: A box {64 ch, 128 px} from the fresh or stale
+//   warp 0      TMA producer (converged warp; an elected lane issues each
+//               copy): A box {64 ch, 128 px} from the fresh or stale
 //               map, B box {64 ch, 1 tap, BN out-ch} of the weights
 //               [C_out][3][3][C_in], 128-byte swizzle, STAGES-deep ring;
-//   warp 1      TMEM owner and single-thread tcgen05.mma issuer
+//   warp 1      TMEM owner and tcgen05.mma issuer (converged warp, one
+//               elected lane per instruction)
 //               (M 128, N BN, K 16), two accumulators 256 columns apart;
 //   warps 2..5  epilogue: tcgen05.ld, + bias (+ the residual already in y
 //               when accumulating), bf16, 16-byte stores; with
@@ -123,7 +125,7 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   const int Hp = p.H / p.P;
 
   if (warp == 0) {
-    if (lane == 0) {  // ---------------------------------------- TMA producer
+    {  // ------------------------- TMA producer (converged warp, elected lane)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
@@ -142,13 +144,13 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           const int hc = (p.zero_halo && halo_row) ? -1 : hh;
           const int ww = w0 + tap % 3 - 1;
           const CUtensorMap *src = (p.use_stale && halo_row) ? &tmS : &tmX;
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
+          if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
           uint8_t *sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          mbar_arrive_expect_tx_w(&full[stage], STAGE_BYTES);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          tma_load_4d(sa, src, &full[stage], cb * BK, ww, hc, b);
-          tma_load_3d(sa + A_BYTES, &tmW, &full[stage], cb * BK, tap, n0);
+          tma_load_4d_w(sa, src, &full[stage], cb * BK, ww, hc, b);
+          tma_load_3d_w(sa + A_BYTES, &tmW, &full[stage], cb * BK, tap, n0);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -160,19 +162,19 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           if ((armed >> s) & 1u) mbar_drain(&full[s], (armed_parity >> s) & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // --------------------------------------- MMA issuer
+    {  // ---------------------------- MMA issuer (converged warp, elected lane)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        if (!mbar_wait_w(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * 256;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+          if (!mbar_wait_w(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -182,18 +184,18 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           const uint64_t bd = desc_sw128_kmajor(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_f16_ss(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0);
-          mma_commit(&empty[stage]);
+            mma_f16_ss_w(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0);
+          mma_commit_w(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        mma_commit_w(&tfull[acc]);
       }
       if (*abort_flag) {
-        mma_commit(drain);
+        mma_commit_w(drain);
         mbar_drain(drain, 0);
       }
     }

@@ -7,10 +7,12 @@
 // refresh of DistriSelfAttentionPP's state costs no extra pass).
 //
 // Persistent, warp-specialised, one CTA per SM:
-//   warp 0      TMA producer: A tile 128 x 64 and B tile BN x 64 per stage
+//   warp 0      TMA producer (the warp stays converged; an elected lane issues
+//               each copy): A tile 128 x 64 and B tile BN x 64 per stage
 //               (B as BN/64 boxes of 64 rows, each from the weight block that
 //               holds it), 128-byte swizzle, STAGES-deep mbarrier ring;
-//   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warp 1      TMEM allocation and the tcgen05.mma issuer (converged warp,
+//               one elected lane per instruction)
 //               (M = 128, N = BN, K = 16 per instruction), fp32 accumulators
 //               double-buffered in TMEM (2 x BN columns);
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, + bias (a per-warp
@@ -127,25 +129,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int tiles = p.m_tiles * p.n_tiles;
 
   if (warp == 0) {
-    if (lane == 0) {  // ---------------------------------------- TMA producer
+    {  // ------------------------- TMA producer (converged warp, elected lane)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;  // per-stage bits, for the abort drain
       for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
         const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
+          if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
           uint8_t *sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          mbar_arrive_expect_tx_w(&full[stage], STAGE_BYTES);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+          tma_load_2d_w(sa, &tmA, &full[stage], kb * BK, m0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j) {
             if (p.geglu) {  // value rows, then the matching gate rows
               const bool gate = j >= BN / 128;
               const int n = n0 / 2 + 64 * (gate ? j - BN / 128 : j);
-              tma_load_2d(sa + A_BYTES + j * 64 * 128, gate ? &tmB1 : &tmB0, &full[stage],
+              tma_load_2d_w(sa + A_BYTES + j * 64 * 128, gate ? &tmB1 : &tmB0, &full[stage],
                           kb * BK, n);
               continue;
             }
@@ -153,7 +155,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int mat = n / p.b_rows;
             if (mat > 2) mat = 2;
             const CUtensorMap *mp = mat == 0 ? &tmB0 : (mat == 1 ? &tmB1 : &tmB2);
-            tma_load_2d(sa + A_BYTES + j * 64 * 128, mp, &full[stage], kb * BK,
+            tma_load_2d_w(sa + A_BYTES + j * 64 * 128, mp, &full[stage], kb * BK,
                         n - mat * p.b_rows);
           }
           if (++stage == STAGES) {
@@ -167,19 +169,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if ((armed >> s) & 1u) mbar_drain(&full[s], (armed_parity >> s) & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // --------------------------------------- MMA issuer
+    {  // ---------------------------- MMA issuer (converged warp, elected lane)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        if (!mbar_wait_w(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+          if (!mbar_wait_w(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -189,18 +191,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint64_t bd = desc_sw128_kmajor(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_f16_ss(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0);
-          mma_commit(&empty[stage]);
+            mma_f16_ss_w(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0);
+          mma_commit_w(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        mma_commit_w(&tfull[acc]);
       }
       if (*abort_flag) {  // no MMA may still be writing TMEM when it is freed
-        mma_commit(drain);
+        mma_commit_w(drain);
         mbar_drain(drain, 0);
       }
     }

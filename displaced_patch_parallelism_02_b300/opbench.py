@@ -6,6 +6,12 @@ profiling needs (ncu -k ... -s <warm-up launches> -c ...).
     python -m displaced_patch_parallelism_02_b300.opbench cfg --n 921600
     python -m displaced_patch_parallelism_02_b300.opbench conv_gn --H 512 --W 512 --C 320 --P 8
     python -m displaced_patch_parallelism_02_b300.opbench layernorm --T 262144 --C 640
+    python -m displaced_patch_parallelism_02_b300.opbench attn --B 2 --H 240 --W 240 --P 8
+
+`attn` is one displaced self-attention call (QKV projection, core, output
+projection); its figure is the attention core alone, timed by the events the
+library records around the core launch (dpp_set_attn_core_events), FLOPs
+4 * B * N^2 * 64 * heads.
 
 Inputs are seeded random device tensors (bf16 activations, weights scaled by
 1/sqrt(fan_in), fp32 guidance maps); `--warmup` calls run first, then `--reps`
@@ -20,9 +26,11 @@ import json
 
 import torch
 
-from . import (DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_cfg_combine, dpp_cfg_workspace_bytes,
-               dpp_conv3x3_gn, dpp_conv_desc, dpp_device_status, dpp_gn_desc,
-               dpp_groupnorm_apply, dpp_layernorm, dpp_linear, dpp_linear_desc, dpp_ln_desc)
+from . import (DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_attn_desc, dpp_cfg_combine,
+               dpp_cfg_workspace_bytes, dpp_conv3x3_gn, dpp_conv_desc, dpp_device_status,
+               dpp_gn_desc, dpp_groupnorm_apply, dpp_layernorm, dpp_linear, dpp_linear_desc,
+               dpp_ln_desc, dpp_self_attn, dpp_self_attn_workspace_bytes,
+               dpp_set_attn_core_events)
 
 
 def _randn(shape, gen, scale=1.0, dtype=torch.bfloat16):
@@ -74,12 +82,33 @@ def setup(args, gen):
         g, b = torch.ones(C, device="cuda"), torch.zeros(C, device="cuda")
         d = dpp_ln_desc(T, C, 1e-5, DPP_BF16)
         return (lambda: dpp_layernorm(d, x, g, b, y)), 2.0 * 2 * T * C, "GB/s"
+    if args.op == "attn":
+        B, H, W, P, heads = args.B, args.H, args.W, args.P, args.heads
+        C, N = 64 * heads, args.H * args.W
+        x = _randn((B, N, C), gen)
+        wq, wk, wv, wo = (_randn((C, C), gen, C ** -0.5) for _ in range(4))
+        kv = [torch.empty((B, N, 2, C), dtype=torch.float16, device="cuda") for _ in range(2)]
+        y = torch.empty_like(x)
+        d = dpp_attn_desc(B, H, W, C, heads, 64, P, 0, 0, DPP_BF16, 0, 0)
+        nws = dpp_self_attn_workspace_bytes(d)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        dpp_self_attn(d, x, wq, wk, wv, wo, None, kv[0], y, ws, nws)  # synchronous step
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for e in ev:  # creates the CUDA events; the library re-records them
+            e.record()
+
+        def call():
+            dpp_set_attn_core_events(*ev)
+            dpp_self_attn(d, x, wq, wk, wv, wo, kv[0], kv[1], y, ws, nws)
+            dpp_set_attn_core_events(None, None)
+        call.core_events = ev
+        return call, 4.0 * B * N * N * 64 * heads, "TFLOP/s"
     raise ValueError(args.op)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm"])
+    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm", "attn"])
     ap.add_argument("--M", type=int, default=115200)
     ap.add_argument("--K", type=int, default=640)
     ap.add_argument("--N", type=int, default=640)
@@ -94,6 +123,7 @@ def main(argv=None):
     ap.add_argument("--P", type=int, default=8)
     ap.add_argument("--G", type=int, default=32)
     ap.add_argument("--T", type=int, default=262144)
+    ap.add_argument("--heads", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--reps", type=int, default=1)
     args = ap.parse_args(argv)
@@ -110,6 +140,9 @@ def main(argv=None):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / max(args.reps, 1)
+    core = getattr(call, "core_events", None)
+    if core is not None and args.reps > 0:  # the last call's attention core alone
+        ms = core[0].elapsed_time(core[1])
     rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
     out = {k: v for k, v in vars(args).items()}
     out.update(ms_per_call=ms, achieved=rate, unit=unit, status=dpp_device_status())
