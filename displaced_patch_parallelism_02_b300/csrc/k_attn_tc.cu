@@ -56,7 +56,9 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;
+constexpr uint32_t OFF_TAB = OFF_BAR + 512;
+constexpr int kTabTiles = 1024;  // key tiles described in shared memory (more: computed)
+constexpr uint32_t SMEM_BYTES = OFF_TAB + kTabTiles * 16 + 1024;
 constexpr float kRescaleThreshold = 4.f;
 
 struct AttnTcParams {
@@ -69,7 +71,7 @@ struct AttnTcParams {
   float scale_log2;
 };
 
-struct KvTile {
+struct __align__(16) KvTile {
   int kv0, vlo, vhi, fresh;
 };
 
@@ -190,6 +192,15 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t bd, ui
       : "memory");
 }
 
+// One elected lane of a converged warp arrives on `bar`.
+__device__ __forceinline__ void mbar_arrive_w(uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // Warp-uniform bounded wait: every lane waits, then the warp agrees.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           int *status) {
@@ -221,12 +232,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int qend = (band + 1) * Np;
   const Segs segs = make_segs(p, band);
   const int T = segs.total;
+  // the band's last CTA may hold a single query tile (the band's tail)
+  const int ntile = q0 + 128 < qend ? 2 : 1;
+  // the key tiles of this band, walked once here instead of in every warp
+  const KvTile *tab = reinterpret_cast<const KvTile *>(smem + OFF_TAB);
+  for (int j = threadIdx.x; j < T && j < kTabTiles; j += blockDim.x)
+    reinterpret_cast<KvTile *>(smem + OFF_TAB)[j] = tile_of(segs, j);
+  auto kv_tile = [&](int j) -> KvTile { return j < kTabTiles ? tab[j] : tile_of(segs, j); };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    // a K or V slot is free once both query tiles' MMAs have read it
-    for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 2); }
-    for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 2); }
+    // a K or V slot is free once every query tile's MMAs have read it
+    for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], ntile); }
+    for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], ntile); }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&s_empty[t], 8);  // one arrival per softmax warp of the tile
@@ -256,11 +274,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     // The whole warp runs the loop (warp-uniform operands); one elected lane
     // issues each copy.
     uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
-    mbar_arrive_expect_tx_w(q_full, 2 * TILE_BYTES);
+    mbar_arrive_expect_tx_w(q_full, ntile * TILE_BYTES);
     tma_load_2d_w(smem + OFF_Q, &tmQ, q_full, head * 64, b * p.Nq + q0);
-    tma_load_2d_w(smem + OFF_Q + TILE_BYTES, &tmQ, q_full, head * 64, b * p.Nq + q0 + 128);
+    if (ntile == 2)
+      tma_load_2d_w(smem + OFF_Q + TILE_BYTES, &tmQ, q_full, head * 64, b * p.Nq + q0 + 128);
     for (int j = 0; j < T; ++j) {
-      const KvTile kt = tile_of(segs, j);
+      const KvTile kt = kv_tile(j);
       const CUtensorMap *m = kt.fresh ? &tmF : &tmS;
       const int row = b * p.Nkv + kt.kv0;
       const int ks = j % KS, vs = j % VS;
@@ -283,7 +302,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int i = 0; i < VS; ++i)
         if ((v_armed >> i) & 1u) mbar_drain(&v_full[i], (v_par >> i) & 1u);
     }
-  } else if (warp == 1 || warp == 2) {  // ------------- MMA issuer of query tile t
+  } else if ((warp == 1 || warp == 2) && warp - 1 < ntile) {  // --- MMA issuer of tile t
     // Each query tile has its own issuing warp, so one tile's wait for its
     // softmax never holds back the other tile's MMAs.  Per key tile j:
     // S(j) = Q K(j)^T as soon as the softmax has read S(j-1), then
@@ -321,7 +340,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       mma_commit_w(&drain[t]);
       mbar_drain(&drain[t], 0);
     }
-  } else {  // ------------------------------------------------------ softmax
+  } else if (warp >= 3 && (warp - 3) >> 3 < ntile) {  // -------------------- softmax
     const int sw = warp - 3;                // 0..15
     const int t = sw >> 3;                  // query tile
     const int quad = warp & 3;              // TMEM lanes this warp may access: 32*quad..
@@ -333,7 +352,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     float m_ref = -INFINITY, l = 0.f;  // l: this thread's half of the row sum
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      const KvTile kt = tile_of(segs, j);
+      const KvTile kt = kv_tile(j);
       if (!warp_wait(&s_full[t], j & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[64];
@@ -341,8 +360,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tmem_ld16x2_32<64>(tS + 32, *reinterpret_cast<uint32_t (*)[32]>(&sr[32]));
       tmem_wait_ld();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[t]);
+      mbar_arrive_w(&s_empty[t]);
       if (kt.vlo != 0 || kt.vhi != 128) {  // ragged tile (uniform branch): mask
         const int k0 = half * 64;
 #pragma unroll
@@ -406,8 +424,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       }
       tmem_wait_st();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
+      mbar_arrive_w(&p_full[t]);
     }
     if (ok && warp_wait(&o_final[t], 0, abort_flag, p.status)) {
       tc_fence_after();
