@@ -31,6 +31,7 @@ DPP_ERR_WORKSPACE = 4
 DPP_ERR_CUDA = 5
 DPP_ERR_TIMEOUT = 6
 DPP_ERR_ALIGN = 7
+DPP_ERR_RANGE = 8
 
 DPP_F32 = 0
 DPP_BF16 = 1

@@ -169,6 +169,7 @@ const char *dpp_status_string(dpp_status s) {
     case DPP_ERR_CUDA: return "DPP_ERR_CUDA";
     case DPP_ERR_TIMEOUT: return "DPP_ERR_TIMEOUT";
     case DPP_ERR_ALIGN: return "DPP_ERR_ALIGN";
+    case DPP_ERR_RANGE: return "DPP_ERR_RANGE";
   }
   return "DPP_ERR_UNKNOWN";
 }

@@ -299,6 +299,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) mbar_arrive(&tempty[acc]);
         continue;
       }
+      float amax = 0.f;  // largest |value| this thread stores (fp16 range check)
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -346,12 +347,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                   b += __uint_as_float(rw[e] & 0xffff0000u);
                 }
               }
+              if (p.out_f16) amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
               ow[e] = p.out_f16 ? pack_half2(a, b) : pack_bf162(a, b);
             }
             dst[v] = o;
           }
         }
       }
+      // An fp16 output (the attention state of a bf16 layer) cannot hold a
+      // value above 65504: such a call is reported, not silently saturated.
+      if (p.out_f16 && __any_sync(0xffffffffu, amax > 65504.f) && lane == 0 && p.status)
+        atomicCAS(p.status, 0, (int)DPP_ERR_RANGE);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);

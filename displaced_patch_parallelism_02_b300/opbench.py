@@ -7,6 +7,8 @@ profiling needs (ncu -k ... -s <warm-up launches> -c ...).
     python -m displaced_patch_parallelism_02_b300.opbench conv_gn --H 512 --W 512 --C 320 --P 8
     python -m displaced_patch_parallelism_02_b300.opbench layernorm --T 262144 --C 640
     python -m displaced_patch_parallelism_02_b300.opbench attn --B 2 --H 240 --W 240 --P 8
+    python -m displaced_patch_parallelism_02_b300.opbench groupnorm --B 2 --H 480 --W 480 \
+        --C 320 --P 8 --flush
 
 `attn` is one displaced self-attention call (QKV projection, core, output
 projection); its figure is the attention core alone, timed by the events the
@@ -15,7 +17,8 @@ library records around the core launch (dpp_set_attn_core_events), FLOPs
 
 Inputs are seeded random device tensors (bf16 activations, weights scaled by
 1/sqrt(fan_in), fp32 guidance maps); `--warmup` calls run first, then `--reps`
-calls between two CUDA events.  Prints one JSON line with the time per call
+calls between two CUDA events (with `--flush`, each rep between its own
+events after a write of twice the L2 size, and the median is reported).  Prints one JSON line with the time per call
 and the achieved TFLOP/s (contractions) or GB/s (read x + write y).
 Every call is the library's own entry point; nothing here computes anything.
 """
@@ -28,7 +31,8 @@ import torch
 
 from . import (DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_attn_desc, dpp_cfg_combine,
                dpp_cfg_workspace_bytes, dpp_conv3x3_gn, dpp_conv_desc, dpp_device_status,
-               dpp_gn_desc, dpp_groupnorm_apply, dpp_layernorm, dpp_linear, dpp_linear_desc,
+               dpp_gn_desc, dpp_groupnorm, dpp_groupnorm_apply, dpp_groupnorm_workspace_bytes,
+               dpp_layernorm, dpp_linear, dpp_linear_desc,
                dpp_ln_desc, dpp_self_attn, dpp_self_attn_workspace_bytes,
                dpp_set_attn_core_events)
 
@@ -103,12 +107,24 @@ def setup(args, gen):
             dpp_set_attn_core_events(None, None)
         call.core_events = ev
         return call, 4.0 * B * N * N * 64 * heads, "TFLOP/s"
+    if args.op == "groupnorm":  # the displaced step, sums of its own input
+        B, H, W, C, P, G = args.B, args.H, args.W, args.C, args.P, args.G
+        x = _randn((B, H, W, C), gen)
+        y = torch.empty_like(x)
+        gamma, beta = torch.ones(C, device="cuda"), torch.zeros(C, device="cuda")
+        d = dpp_gn_desc(B, H, W, C, G, P, 1e-5, DPP_BF16, 0, 0)
+        nws = dpp_groupnorm_workspace_bytes(d)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        st = [torch.empty((P, B, G, 2), device="cuda") for _ in range(2)]
+        dpp_groupnorm(d, x, None, st[0], gamma, beta, y, ws, nws)  # synchronous step
+        return (lambda: dpp_groupnorm(d, x, st[0], st[1], gamma, beta, y, ws, nws),
+                2.0 * B * H * W * C * 2, "GB/s")
     raise ValueError(args.op)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm", "attn"])
+    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm", "attn", "groupnorm"])
     ap.add_argument("--M", type=int, default=115200)
     ap.add_argument("--K", type=int, default=640)
     ap.add_argument("--N", type=int, default=640)
@@ -126,6 +142,8 @@ def main(argv=None):
     ap.add_argument("--heads", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--reps", type=int, default=1)
+    ap.add_argument("--flush", action="store_true",
+                    help="evict L2 before every timed call (cold-cache figure)")
     args = ap.parse_args(argv)
     assert torch.cuda.is_available(), "opbench needs a CUDA device"
     gen = torch.Generator(device="cuda").manual_seed(1234)
@@ -133,13 +151,28 @@ def main(argv=None):
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.reps):
-        call()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / max(args.reps, 1)
+    if args.flush:
+        import statistics
+        l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20))
+        buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
+        times = []
+        for _ in range(max(args.reps, 1)):
+            buf.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+    else:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.reps):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / max(args.reps, 1)
     core = getattr(call, "core_events", None)
     if core is not None and args.reps > 0:  # the last call's attention core alone
         ms = core[0].elapsed_time(core[1])

@@ -47,7 +47,13 @@
  *     and return a dpp_status with no side effect.  A failed launch returns
  *     DPP_ERR_CUDA.  Kernels that wait on barriers give up after a bounded
  *     time and record DPP_ERR_TIMEOUT in a device status word read by
- *     dpp_device_status().
+ *     dpp_device_status(); an attention layer of type DPP_BF16 whose Q, K
+ *     or V leaves the fp16 range records DPP_ERR_RANGE there.
+ *   - Devices: the library keeps, per device, the address of its device
+ *     status word and of the static GroupNorm scratch, and the shared-memory
+ *     limits it has set on its kernels.  These belong to the device's
+ *     primary context: do not use the library across cudaDeviceReset
+ *     (reload the library in a new process instead).
  *   - Synchronous step: passing NULL as the stale input (stale_prev,
  *     stats_prev, kv_prev) means "all bands are fresh" -- the synchronous
  *     first step, which is exactly the unpartitioned full-image layer.
@@ -76,7 +82,10 @@ typedef enum {
   DPP_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
   DPP_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
   DPP_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up */
-  DPP_ERR_ALIGN = 7        /* a pointer is not 16-byte aligned */
+  DPP_ERR_ALIGN = 7,       /* a pointer is not 16-byte aligned */
+  DPP_ERR_RANGE = 8        /* a value exceeded the fp16 range of an attention state
+                              (|Q|, |K| or |V| > 65504 in a bf16 layer); reported
+                              through the device status word */
 } dpp_status;
 
 typedef enum { DPP_F32 = 0, DPP_BF16 = 1 } dpp_dtype;
@@ -270,6 +279,9 @@ dpp_status dpp_groupnorm_apply(const dpp_gn_desc *desc, const void *x, const flo
  *   kv_next  : [B, N, 2, C] output, same type; must not overlap kv_prev.
  *   ws       : dpp_self_attn_workspace_bytes(desc) bytes (Q and O).
  * Requires head_dim == 64, H % P == 0, C == heads * 64.
+ * DPP_BF16 layers hold Q, K, V and O in fp16: if a projected value exceeds
+ * 65504 the call still completes, and DPP_ERR_RANGE is recorded in the
+ * device status word (dpp_device_status); the output is then not valid.
  * ------------------------------------------------------------------------- */
 dpp_status dpp_self_attn(const dpp_attn_desc *desc, const void *x, const void *wq,
                          const void *wk, const void *wv, const void *wo,
@@ -415,7 +427,9 @@ void dpp_switch_init(dpp_switch_state *state, double flat_tol, double rise_tol, 
 int dpp_switch_update(dpp_switch_state *state, double d);
 
 /* Reads and clears the device status word written by bounded waits
- * (DPP_OK or DPP_ERR_TIMEOUT).  Synchronises `stream`. */
+ * (DPP_ERR_TIMEOUT) and by the fp16 range check of bf16 attention layers
+ * (DPP_ERR_RANGE); DPP_OK when neither happened since the last read.
+ * Synchronises `stream`. */
 dpp_status dpp_device_status(dpp_stream stream);
 
 /* Number of kernels this library has launched in this process (monotonic).

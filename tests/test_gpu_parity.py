@@ -199,6 +199,31 @@ def test_groupnorm_never_uses_own_band_of_stale_state(cuda_device):
         assert not torch.equal(y, base)
 
 
+@pytest.mark.parametrize("dt,lo,hi", [(BF16, 30.0, 100.0), (F32, 10.0, 20.0)])
+def test_groupnorm_large_group_means(cuda_device, dt, lo, hi):
+    """Groups whose mean is tens of standard deviations (a conv output with
+    a large bias): the variance must not cancel away.  Every group gets its
+    own mean in [lo, hi] (sign alternating), unit spread; synchronous step,
+    then the displaced step on its published partials, against the oracle.
+    The published state is fp32 (sum x, sum x^2), whose 2^-24 relative
+    precision bounds the variance to about 6e-8 (mean / sd)^2: the fp32 case
+    stays at means of 10-20 sd, inside the 1e-4 RMS bar."""
+    B, H, W, C, Gn, P = 2, 16, 12, 320, 32, 4
+    g = torch.Generator().manual_seed(404)
+    means = (lo + (hi - lo) * torch.rand(Gn, generator=g)) * torch.tensor(
+        [(-1.0) ** k for k in range(Gn)])
+    shift = means.repeat_interleave(C // Gn)
+    F = (draw((B, H, W, C), 405, F32) + shift).to(dt)
+    S = (wl.perturbed(F.float(), 406, 0.05)).to(dt)
+    gamma, beta = wl.gn_affine(C, 8)
+    y_s, stats_s = G.groupnorm(S, None, Gn, 1e-5, gamma, beta, P)
+    y, _ = G.groupnorm(F, stats_s, Gn, 1e-5, gamma, beta, P)
+    ref_s = oracle.groupnorm(G.f64(S), Gn, 1e-5, G.f64(gamma), G.f64(beta))
+    G.assert_rms_close(G.f64(y_s), ref_s, G.TOL[dt], "gn sync, large means")
+    ref = oracle.displaced_groupnorm(G.f64(F), G.f64(S), Gn, 1e-5, G.f64(gamma), G.f64(beta), P)
+    G.assert_rms_close(G.f64(y), ref, G.TOL[dt], "gn displaced, large means")
+
+
 # ---------------------------------------------------------------- attention
 ATTN_CASES = [  # (B, H, W, heads, P, dtype)
     (1, 32, 32, 1, 2, F32),     # the tiny fp32 workload
@@ -262,6 +287,28 @@ def test_cross_attn_matches_oracle(cuda_device, B, H, W, heads, n_ctx, c_ctx, dt
     ref = oracle.cross_attention(G.f64(X), G.f64(ctx), w64["wq"], w64["wk"], w64["wv"],
                                  w64["wo"], heads)
     G.assert_rms_close(G.f64(y), ref, G.TOL[dt], "cross-attn")
+
+
+def test_bf16_attention_reports_fp16_range(cuda_device):
+    """A bf16 attention layer holds Q, K and V in fp16.  Inputs large enough
+    that a projected K exceeds 65504 are reported as DPP_ERR_RANGE in the
+    device status word (the call completes; its output is not valid), and
+    the status is clean again for the next, in-range call."""
+    B, H, W, heads, P = 1, 8, 8, 1, 2
+    a = wl.AttnShape(B, H, W, 64, heads, 64, P)
+    wts = wl.attn_weights(a, 9, "bf16")
+    F = draw((B, H * W, 64), 501, BF16)
+    kmax = float(np.abs(G.f64(F) @ G.f64(wts["wk"]).T).max())
+    assert G.dpp.dpp_device_status() == G.dpp.DPP_OK
+    big = (F.float() * (1.0e5 / kmax)).to(BF16)  # largest |K| about 1e5
+    G.self_attn(big, wts, None, H, W, heads, P)
+    assert G.dpp.dpp_device_status() == G.dpp.DPP_ERR_RANGE
+    y, _ = G.self_attn(F, wts, None, H, W, heads, P)
+    assert G.dpp.dpp_device_status() == G.dpp.DPP_OK
+    w64 = {k: G.f64(v) for k, v in wts.items()}
+    ref = oracle.displaced_self_attention(G.f64(F), G.f64(F), w64["wq"], w64["wk"], w64["wv"],
+                                          w64["wo"], heads, P)
+    G.assert_rms_close(G.f64(y), ref, G.TOL[BF16], "in-range call after the range error")
 
 
 def test_no_device_timeouts_recorded(cuda_device):
