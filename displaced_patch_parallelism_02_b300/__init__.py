@@ -129,6 +129,7 @@ _SIGNATURES = {
     "dpp_device_status": (_st, [_vp]),
     "dpp_status_string": (ctypes.c_char_p, [_st]),
     "dpp_version": (ctypes.c_int, []),
+    "dpp_source_hash": (ctypes.c_char_p, []),
     "dpp_launch_count": (ctypes.c_uint64, []),
     "dpp_set_attn_core_events": (None, [_vp, _vp]),
     "dpp_workspace_bytes": (_sz, [ctypes.c_int, _vp]),
@@ -178,6 +179,10 @@ def dpp_status_string(status: int) -> str:
 
 def dpp_version() -> int:
     return lib.dpp_version()
+
+
+def dpp_source_hash() -> str:
+    return lib.dpp_source_hash().decode()
 
 
 def dpp_launch_count() -> int:

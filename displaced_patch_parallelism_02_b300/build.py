@@ -7,7 +7,10 @@ about to be rebuilt)
 
 Each translation unit in csrc/ is compiled to an object under
 csrc/_build/ in parallel, then linked into libdpp.so next to this file.
-Nothing is rebuilt when every object is newer than its sources and headers.
+A SHA-256 of the sources, headers and compiler flags is compiled into the
+library (dpp_source_hash()); a library whose hash differs from the current
+sources is rebuilt whatever its file times say, and objects are reused only
+when newer than their sources and built with the same hash.
 """
 from __future__ import annotations
 
@@ -41,6 +44,29 @@ def _headers():
         [os.path.join(ROOT, "include", "dpp.h")]
 
 
+def source_hash() -> str:
+    """SHA-256 of every source, header and the compiler flags."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(CSRC, "*.cu"))) + sorted(_headers()):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + FLAGS).encode())
+    return h.hexdigest()
+
+
+def library_hash(lib: str = LIB):
+    """The hash compiled into an existing libdpp.so, read in a child process
+    (so this process does not keep the library loaded), or None."""
+    if not os.path.exists(lib):
+        return None
+    code = ("import ctypes, sys; l = ctypes.CDLL(sys.argv[1]); "
+            "f = l.dpp_source_hash; f.restype = ctypes.c_char_p; print(f().decode())")
+    r = subprocess.run([sys.executable, "-c", code, lib], capture_output=True, text=True)
+    return r.stdout.strip() if r.returncode == 0 else None
+
+
 def _stale(target: str, deps) -> bool:
     if not os.path.exists(target):
         return True
@@ -52,14 +78,21 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdrs = _headers()
+    want = source_hash()
+    stamp = os.path.join(BUILD, "source_hash")
+    built_with = open(stamp).read().strip() if os.path.exists(stamp) else None
+    if built_with != want:  # objects from other sources or flags: rebuild them all
+        force = True
+    if not force and library_hash() != want:
+        force = True  # a library whose embedded hash does not match these sources
     jobs = []
     objs = []
     for s in srcs:
         o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
-            cmd = [nvcc()] + ARCH + FLAGS + (["-Xptxas", "-v"] if verbose_ptxas else []) + \
-                ["-c", s, "-o", o]
+            cmd = [nvcc()] + ARCH + FLAGS + [f"-DDPP_SOURCE_SHA256=\"{want}\""] + \
+                (["-Xptxas", "-v"] if verbose_ptxas else []) + ["-c", s, "-o", o]
             jobs.append(cmd)
 
     def run(cmd):
@@ -84,6 +117,8 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
+    with open(stamp, "w") as fh:
+        fh.write(want)
     return LIB
 
 

@@ -176,6 +176,11 @@ const char *dpp_status_string(dpp_status s) {
 
 int dpp_version(void) { return 100; }
 
+#ifndef DPP_SOURCE_SHA256
+#define DPP_SOURCE_SHA256 "unknown"
+#endif
+const char *dpp_source_hash(void) { return DPP_SOURCE_SHA256; }
+
 uint64_t dpp_launch_count(void) { return g_launches.load(); }
 
 void dpp_set_attn_core_events(void *start, void *stop) {

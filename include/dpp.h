@@ -432,6 +432,10 @@ int dpp_switch_update(dpp_switch_state *state, double d);
  * Synchronises `stream`. */
 dpp_status dpp_device_status(dpp_stream stream);
 
+/* SHA-256 (hex) of the sources and compiler flags this library was built
+ * from; the build rebuilds a library whose hash differs from its sources. */
+const char *dpp_source_hash(void);
+
 /* Number of kernels this library has launched in this process (monotonic).
  * Calls rejected by argument checks launch nothing and leave it unchanged. */
 uint64_t dpp_launch_count(void);

@@ -332,3 +332,17 @@ def test_opbench_parses_its_options_and_needs_a_device():
     if not torch.cuda.is_available():
         with pytest.raises(AssertionError, match="CUDA device"):
             opbench.main(["linear", "--M", "128"])
+
+
+def test_library_is_built_from_these_sources():
+    """The library carries the SHA-256 of the sources and flags it was built
+    from; build() rebuilds it when that differs from the files here, so a
+    prebuilt library cannot stand in for edited sources."""
+    import importlib.util
+    path = os.path.join(ROOT, "displaced_patch_parallelism_02_b300", "build.py")
+    spec = importlib.util.spec_from_file_location("_dpp_build_check", path)
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    assert dpp.dpp_source_hash() == b.source_hash()
+    assert b.library_hash() == b.source_hash()
+    assert b.library_hash(os.path.join(ROOT, "no_such_library.so")) is None
