@@ -79,6 +79,7 @@ template <int BN, int STAGES, bool IN_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+               const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                const GemmTcParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
@@ -135,15 +136,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t armed = 0, armed_parity = 0;  // per-stage bits, for the abort drain
       for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
         const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
+        // 64-row boxes of B this tile needs (a ragged last tile of a plain
+        // GEMM loads, and multiplies, only its own columns)
+        const int nbox = p.geglu ? BN / 64 : min(BN / 64, (p.N - n0 + 63) / 64);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
           uint8_t *sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx_w(&full[stage], STAGE_BYTES);
+          mbar_arrive_expect_tx_w(&full[stage], A_BYTES + nbox * 64 * BK * 2);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           tma_load_2d_w(sa, &tmA, &full[stage], kb * BK, m0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j) {
+            if (j >= nbox) break;
             if (p.geglu) {  // value rows, then the matching gate rows
               const bool gate = j >= BN / 128;
               const int n = n0 / 2 + 64 * (gate ? j - BN / 128 : j);
@@ -179,6 +184,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!mbar_wait_w(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
+        const int n0 = (t % p.n_tiles) * BN;
+        const uint32_t idesc =
+            p.geglu ? IDESC : idesc_f16(BM, 64 * min(BN / 64, (p.N - n0 + 63) / 64), IN_BF16);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_w(&full[stage], phase, abort_flag, p.status)) {
@@ -191,7 +199,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint64_t bd = desc_sw128_kmajor(sa + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_f16_ss_w(d, ad + 2 * k, bd + 2 * k, IDESC, (kb | k) != 0);
+            mma_f16_ss_w(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
           mma_commit_w(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -211,6 +219,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int row = q * 32 + lane;
     // this warp's copy of the tile's bias (gated GELU: value bias, then gate bias)
     float *bias_s = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + 512) + q * BN;
+    // this warp's two output staging buffers (32 rows x 32 columns of 16-bit
+    // values each) for the bulk tensor stores
+    uint8_t *stage_o = smem + STAGES * STAGE_BYTES + 512 + 4 * BN * sizeof(float) + q * 4096;
+    int n_stored = 0;  // chunks this warp has handed to the bulk-store engine
     constexpr int PRE = BN <= 128 ? BN / 8 : 1;  // residual vectors a thread prefetches
     int it = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
@@ -300,17 +312,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         continue;
       }
       float amax = 0.f;  // largest |value| this thread stores (fp16 range check)
+      // Each 32 x 32 chunk is converted into a staging buffer (row = lane,
+      // 64 bytes) and written by one bulk tensor store: whole cache lines,
+      // asynchronous, rows past M clipped by the tensor map.  With a
+      // residual to add, the next chunk's residual loads are issued before
+      // this chunk is converted, so their latency overlaps the work.
+      auto residual = [&](int c, uint4 (&rr)[4]) {
+        const int n = n0 + c * 32;
+        const bool ld = p.accumulate && m < p.M && n < p.N && n < p.split;
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          rr[v] = ld ? reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.out0) +
+                                                       (size_t)m * p.ld0 + n)[v]
+                     : make_uint4(0u, 0u, 0u, 0u);
+      };
+      uint4 res_next[4];
+      if constexpr (BN > 128) residual(0, res_next);
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
         const int n = n0 + c * 32;
-        const bool in = m < p.M && n < p.N;
+        const bool col_in = n < p.N;
         const bool first = n < p.split;
-        uint4 *dst = first ? reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out0) +
-                                                       (size_t)m * p.ld0 + n)
-                           : reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out1) +
-                                                       (size_t)m * p.ld1 + (n - p.split));
         const bool acc_in = first && p.accumulate;
         uint4 res[4];  // the residual already in out0
         if constexpr (BN <= 128) {
@@ -318,41 +342,50 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int v = 0; v < 4; ++v) res[v] = pre[c * 4 + v];
         } else {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            res[v] = in && acc_in ? dst[v] : make_uint4(0u, 0u, 0u, 0u);
+          for (int v = 0; v < 4; ++v) res[v] = res_next[v];
+          if (c + 1 < BN / 32) residual(c + 1, res_next);
         }
         tmem_wait_ld();
-        if (in) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
-            const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k = v * 8 + 2 * e;
-              float a = __uint_as_float(r[k]);
-              float b = __uint_as_float(r[k + 1]);
-              if (p.bias) {  // zero outside out0's columns
-                a += bias_s[c * 32 + k];
-                b += bias_s[c * 32 + k + 1];
-              }
-              if (acc_in) {  // out0 is bf16 or fp16, as the output
-                if (p.out_f16) {
-                  const float2 old = __half22float2(*reinterpret_cast<const __half2 *>(&rw[e]));
-                  a += old.x;
-                  b += old.y;
-                } else {
-                  a += __uint_as_float(rw[e] << 16);
-                  b += __uint_as_float(rw[e] & 0xffff0000u);
-                }
-              }
-              if (p.out_f16) amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
-              ow[e] = p.out_f16 ? pack_half2(a, b) : pack_bf162(a, b);
-            }
-            dst[v] = o;
-          }
+        if (!col_in) continue;  // warp-uniform: the whole chunk lies past N
+        uint8_t *buf = stage_o + (n_stored & 1) * 2048;
+        if (n_stored >= 2) {  // the store that read this buffer two chunks ago
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
         }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 o;
+          uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+          const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = v * 8 + 2 * e;
+            float a = __uint_as_float(r[k]);
+            float b = __uint_as_float(r[k + 1]);
+            if (p.bias) {  // zero outside out0's columns
+              a += bias_s[c * 32 + k];
+              b += bias_s[c * 32 + k + 1];
+            }
+            if (acc_in) {  // out0 is bf16 or fp16, as the output
+              if (p.out_f16) {
+                const float2 old = __half22float2(*reinterpret_cast<const __half2 *>(&rw[e]));
+                a += old.x;
+                b += old.y;
+              } else {
+                a += __uint_as_float(rw[e] << 16);
+                b += __uint_as_float(rw[e] & 0xffff0000u);
+              }
+            }
+            if (p.out_f16) amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+            ow[e] = p.out_f16 ? pack_half2(a, b) : pack_bf162(a, b);
+          }
+          *reinterpret_cast<uint4 *>(buf + lane * 64 + v * 16) = o;
+        }
+        fence_proxy_async_smem();  // the generic-proxy writes, before the bulk copy reads them
+        __syncwarp();
+        if (lane == 0)  // lane 0 issues, and later waits for, this warp's stores
+          tma_store_2d(first ? &tmO0 : &tmO1, buf, first ? n : n - p.split, m0 + q * 32);
+        ++n_stored;
       }
       // An fp16 output (the attention state of a bf16 layer) cannot hold a
       // value above 65504: such a call is reported, not silently saturated.
@@ -362,6 +395,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
+    if (lane == 0) bulk_wait_all();  // every bulk store has landed before the CTA exits
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -391,13 +426,33 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
     if (!encode_tiled(&mb[i], ty, 2, b, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  // output tensor maps (16-bit, 32 x 32 boxes, no swizzle): out0 holds columns
+  // [0, split) (all N without a second destination), out1 columns [split, N)
+  CUtensorMap mo[2];
+  {
+    const CUtensorMapDataType to = tma_type(g.to);
+    const int w0 = g.out1 ? g.split : g.N;
+    const uint64_t d0[2] = {(uint64_t)w0, (uint64_t)g.M};
+    const uint64_t s0[1] = {(uint64_t)g.ld0 * 2};
+    const uint32_t box[2] = {32, 32};
+    if (!encode_tiled(&mo[0], to, 2, g.out0, d0, s0, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    mo[1] = mo[0];
+    if (g.out1 && g.N > g.split) {
+      const uint64_t d1[2] = {(uint64_t)(g.N - g.split), (uint64_t)g.M};
+      const uint64_t s1[1] = {(uint64_t)g.ld1 * 2};
+      if (!encode_tiled(&mo[1], to, 2, g.out1, d1, s1, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    }
+  }
   const int n_cols = g.geglu ? 2 * g.N : g.N;  // accumulator columns in all
   GemmTcParams p{g.M, g.N, g.K, g.b_rows, g.out0, g.ld0, g.split, g.out1, g.ld1,
                  g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, (n_cols + BN - 1) / BN, status,
                  g.bias, g.accumulate ? 1 : 0, g.geglu ? 1 : 0};
-  // stages, 1024-byte alignment slack, barriers, the epilogue warps' bias slices
-  constexpr size_t smem =
-      (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512 + 4 * BN * sizeof(float);
+  // stages, 1024-byte alignment slack, barriers, the epilogue warps' bias
+  // slices and output staging buffers
+  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512 +
+                          4 * BN * sizeof(float) + 4 * 4096;
   auto k = gemm_tc_kernel<BN, STAGES, IN_BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -406,7 +461,7 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < sms ? tiles : sms;
-  k<<<grid, kThreads, smem, s>>>(ma, mb[0], mb[1], mb[2], p);
+  k<<<grid, kThreads, smem, s>>>(ma, mb[0], mb[1], mb[2], mo[0], mo[1], p);
   return cudaGetLastError();
 }
 
@@ -471,11 +526,9 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s) {
       return bf ? run<256, 4, true>(g, status, s) : run<256, 4, false>(g, status, s);
     return bf ? run<128, 6, true>(g, status, s) : run<128, 6, false>(g, status, s);
   }
-  if (g.N % 192 == 0)
-    return bf ? run<192, 5, true>(g, status, s) : run<192, 5, false>(g, status, s);
-  if (g.N % 256 == 0)
-    return bf ? run<256, 4, true>(g, status, s) : run<256, 4, false>(g, status, s);
-  return bf ? run<128, 6, true>(g, status, s) : run<128, 6, false>(g, status, s);
+  // 256-column tiles: each 48 KB stage feeds 512 cycles of MMA (a 128-column
+  // tile's 32 KB feed 256), and a ragged last tile runs a narrower MMA
+  return bf ? run<256, 4, true>(g, status, s) : run<256, 4, false>(g, status, s);
 }
 
 }  // namespace dpp

@@ -283,6 +283,31 @@ __device__ __forceinline__ void tma_load_4d_w(void *dst, const CUtensorMap *map,
       : "memory");
 }
 
+// Shared -> global tiled bulk store (2-D) by the calling thread, committed
+// as a bulk async-group of that thread (wait for it with bulk_wait_read /
+// bulk_wait_all from the same thread).  Elements outside the tensor map's
+// extent are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Wait until at most N of this thread's bulk async-groups still read shared
+// memory (their source buffers before that are free to reuse).
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until all of this thread's bulk async-groups have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Bounded wait by a whole warp: every lane polls, then the warp agrees, so
 // the warp stays converged after it.
 __device__ __forceinline__ bool mbar_wait_w(uint64_t *bar, uint32_t parity,
