@@ -11,7 +11,8 @@ A step runs, through the C ABI, on the SDXL-3840px-with-guidance workload
      10 heads of 64: QKV projection writing the fresh K/V
      state, attention core, output projection             (dpp_self_attn)
   4. cross-attention of the result over 77 x 2048 text
-     context tokens                                        (dpp_cross_attn)
+     context tokens, whose K/V were projected once per
+     prompt at set-up                                      (dpp_cross_attn_cached)
   5. guidance combine + rel-MAE sums, 2 x [4,480,480] fp32 (dpp_cfg_combine)
   6. refresh of the conv's stale buffer with this step's
      input (the all_gather)                                (dpp_refresh_stale)
@@ -73,16 +74,18 @@ def work_model(w):
     proj = 2.0 * a.B * a.N * a.C * 3 * a.C + 2.0 * a.B * a.N * a.C * a.C
     cross = a.n_ctx > 0
     xq_o = 2.0 * 2.0 * a.B * a.N * a.C * a.C if cross else 0.0
+    # the context's K/V are projected once per prompt (dpp_cross_attn_kv),
+    # not per denoising step: counted apart
     xkv = 2.0 * a.B * a.n_ctx * a.c_ctx * 2 * a.C
     xcore = 4.0 * a.B * a.N * a.n_ctx * a.head_dim * a.heads
     act_bytes = c.B * c.H * c.W * c.C * 2
     n_cfg = int(np.prod(w.cfg_shape)) if w.cfg_shape else 0
     return {
         "conv_flop": conv, "self_core_flop": core, "self_proj_flop": proj,
-        "cross_flop": xq_o + xkv + xcore, "cross_core_flop": xcore,
+        "cross_flop": xq_o + xcore, "cross_core_flop": xcore, "cross_kv_flop_per_prompt": xkv,
         "gn_bytes": 2.0 * act_bytes, "refresh_bytes": 2.0 * act_bytes,
         "cfg_bytes": 3.0 * 4 * n_cfg,
-        "step_flop": conv + core + proj + xq_o + xkv + xcore,
+        "step_flop": conv + core + proj + xq_o + xcore,
     }
 
 
@@ -291,9 +294,12 @@ class ConfigOps:
                 self.ctx = put(wl.context(a, w.index, w.dtype))
                 self.xd = dpp.dpp_attn_desc(a.B, a.H, a.W, a.C, a.heads, a.head_dim, 1, a.n_ctx,
                                             a.c_ctx, self.code)
-                self.xws_n = dpp.dpp_cross_attn_workspace_bytes(self.xd)
-                self.xws = torch.empty(self.xws_n, dtype=torch.uint8, device=dev)
+                self.xcws_n = dpp.dpp_cross_attn_cached_workspace_bytes(self.xd)
+                self.xcws = torch.empty(self.xcws_n, dtype=torch.uint8, device=dev)
                 self.yc = torch.empty_like(self.ya)
+                self.kvc = torch.empty((a.B, a.n_ctx, 2, a.C), dtype=kvt, device=dev)
+                dpp.dpp_cross_attn_kv(self.xd, self.ctx, self.xw["wk"], self.xw["wv"], self.kvc,
+                                      stream=self.s)
             # K/V state of the previous step: a synchronous call fills it
             dpp.dpp_self_attn(self.ad, self.xa, self.aw["wq"], self.aw["wk"], self.aw["wv"],
                               self.aw["wo"], None, self.kv[0], self.ya, self.aws, self.aws_n,
@@ -367,12 +373,20 @@ class ConfigOps:
             out["self_attn_projections"] = tensor_op(proj_f, ms - cms,
                                                      entry="QKV + output projections")
             if self.cross:
-                xf = (2.0 * 2.0 * a.B * a.N * a.C * a.C + 2.0 * a.B * a.n_ctx * a.c_ctx * 2 * a.C
+                xf = (2.0 * 2.0 * a.B * a.N * a.C * a.C
                       + 4.0 * a.B * a.N * a.n_ctx * a.head_dim * a.heads)
-                ms = timed(lambda: dpp.dpp_cross_attn(
-                    self.xd, self.ya, self.ctx, self.xw["wq"], self.xw["wk"], self.xw["wv"],
-                    self.xw["wo"], self.yc, self.xws, self.xws_n, stream=s), s, reps)
-                out["cross_attn"] = tensor_op(xf, ms, entry="dpp_cross_attn")
+                kvf = 2.0 * a.B * a.n_ctx * a.c_ctx * 2 * a.C
+                core = core_event_pair(s)
+                ms, cms = timed(lambda: dpp.dpp_cross_attn_cached(
+                    self.xd, self.ya, self.kvc, self.xw["wq"], self.xw["wo"], self.yc,
+                    self.xcws, self.xcws_n, stream=s), s, reps, core=core)
+                out["cross_attn"] = tensor_op(xf, ms, entry="dpp_cross_attn_cached (per step)")
+                out["cross_attn_core"] = tensor_op(4.0 * a.B * a.N * a.n_ctx * a.head_dim * a.heads,
+                                                   cms, entry="attention core over 77 keys")
+                ms = timed(lambda: dpp.dpp_cross_attn_kv(self.xd, self.ctx, self.xw["wk"],
+                                                         self.xw["wv"], self.kvc, stream=s),
+                           s, reps)
+                out["cross_attn_kv"] = tensor_op(kvf, ms, entry="dpp_cross_attn_kv (per prompt)")
         if self.has_cfg:
             ms = timed(lambda: dpp.dpp_cfg_combine(self.u, self.cm, w.cfg_scale, self.n_cfg,
                                                    self.cfg_out, self.csums, self.cws,
@@ -445,8 +459,15 @@ class Step:
                                             a.n_ctx, a.c_ctx, dpp.DPP_BF16)
         self.sa_ws_n = dpp.dpp_self_attn_workspace_bytes(self.attn_desc)
         self.sa_ws = torch.empty(self.sa_ws_n, dtype=torch.uint8, device=dev)
-        self.xa_ws_n = dpp.dpp_cross_attn_workspace_bytes(self.cross_desc) if self.cross else 0
+        self.xa_ws_n = (dpp.dpp_cross_attn_cached_workspace_bytes(self.cross_desc)
+                        if self.cross else 0)
         self.xa_ws = torch.empty(max(self.xa_ws_n, 16), dtype=torch.uint8, device=dev)
+        # the prompt's context K/V, projected once (the context is the same
+        # at every denoising step)
+        self.kv_ctx = torch.empty((a.B, max(a.n_ctx, 1), 2, a.C), dtype=torch.float16, device=dev)
+        if self.cross:
+            dpp.dpp_cross_attn_kv(self.cross_desc, self.ctx, self.xw["wk"], self.xw["wv"],
+                                  self.kv_ctx, stream=self.stream)
         self.kv = [torch.empty((a.B, a.N, 2, a.C), dtype=torch.float16, device=dev)
                    for _ in range(2)]  # fp16 K/V state of a bf16 attention layer
         self.ya = torch.empty((a.B, a.N, a.C), dtype=bf, device=dev)
@@ -498,10 +519,9 @@ class Step:
         if core_events:
             dpp.dpp_set_attn_core_events(None, None)
         rec(3)
-        if self.cross:
-            dpp.dpp_cross_attn(self.cross_desc, self.ya, self.ctx, self.xw["wq"],
-                               self.xw["wk"], self.xw["wv"], self.xw["wo"], self.yc, self.xa_ws,
-                               self.xa_ws_n, stream=s)
+        if self.cross:  # the prompt's context K/V from set-up
+            dpp.dpp_cross_attn_cached(self.cross_desc, self.ya, self.kv_ctx, self.xw["wq"],
+                                      self.xw["wo"], self.yc, self.xa_ws, self.xa_ws_n, stream=s)
         rec(4)
         if self.has_cfg:
             dpp.dpp_cfg_combine(self.u, self.c, w.cfg_scale, self.n_cfg, self.cfg_out,
@@ -527,7 +547,7 @@ class Step:
 
     # The step's inputs copied in and results copied out each end-to-end step;
     # two device sets, so one step's copies overlap the other set's compute.
-    IO = ("x", "xa", "ctx", "u", "c", "y2", "yc", "cfg_out", "sums")
+    IO = ("x", "xa", "u", "c", "y2", "yc", "cfg_out", "sums")
 
     def make_io_sets(self):
         self._sets = [{n: getattr(self, n) for n in self.IO},
@@ -541,11 +561,10 @@ class Step:
         with torch.cuda.stream(stream):
             self.x.copy_(self.host_x, non_blocking=True)
             self.xa.copy_(self.host_xa, non_blocking=True)
-            self.ctx.copy_(self.host_ctx, non_blocking=True)
             self.u.copy_(self.host_u, non_blocking=True)
             self.c.copy_(self.host_c, non_blocking=True)
         return sum(t.numel() * t.element_size() for t in
-                   (self.host_x, self.host_xa, self.host_ctx, self.host_u, self.host_c))
+                   (self.host_x, self.host_xa, self.host_u, self.host_c))
 
     def alloc_d2h(self):
         self.out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)

@@ -123,6 +123,10 @@ _SIGNATURES = {
     "dpp_cross_attn": (_st, [ctypes.POINTER(dpp_attn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                              _vp, _sz, _vp]),
     "dpp_cross_attn_workspace_bytes": (_sz, [ctypes.POINTER(dpp_attn_desc)]),
+    "dpp_cross_attn_kv": (_st, [ctypes.POINTER(dpp_attn_desc), _vp, _vp, _vp, _vp, _vp]),
+    "dpp_cross_attn_cached": (_st, [ctypes.POINTER(dpp_attn_desc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _sz, _vp]),
+    "dpp_cross_attn_cached_workspace_bytes": (_sz, [ctypes.POINTER(dpp_attn_desc)]),
     "dpp_cfg_combine": (_st, [_vp, _vp, ctypes.c_float, _sz, _vp, _vp, _vp, _sz, _vp]),
     "dpp_cfg_workspace_bytes": (_sz, [_sz]),
     "dpp_refresh_stale": (_st, [_vp, _vp, _sz, _sz, _sz, ctypes.c_int, ctypes.c_uint64, _vp]),
@@ -308,6 +312,25 @@ def dpp_cross_attn(desc: dpp_attn_desc, x, ctx, wq, wk, wv, wo, y, ws, ws_bytes,
                                      _ptr(wk), _ptr(wv), _ptr(wo), _ptr(y), _ptr(ws),
                                      int(ws_bytes), _stream(stream)),
                   "dpp_cross_attn", raise_on_error)
+
+
+def dpp_cross_attn_kv(desc: dpp_attn_desc, ctx, wk, wv, kv_ctx, stream=None,
+                      raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_cross_attn_kv(ctypes.byref(desc), _ptr(ctx), _ptr(wk), _ptr(wv),
+                                        _ptr(kv_ctx), _stream(stream)),
+                  "dpp_cross_attn_kv", raise_on_error)
+
+
+def dpp_cross_attn_cached_workspace_bytes(desc: dpp_attn_desc) -> int:
+    return lib.dpp_cross_attn_cached_workspace_bytes(ctypes.byref(desc))
+
+
+def dpp_cross_attn_cached(desc: dpp_attn_desc, x, kv_ctx, wq, wo, y, ws, ws_bytes, stream=None,
+                          raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_cross_attn_cached(ctypes.byref(desc), _ptr(x), _ptr(kv_ctx), _ptr(wq),
+                                            _ptr(wo), _ptr(y), _ptr(ws), int(ws_bytes),
+                                            _stream(stream)),
+                  "dpp_cross_attn_cached", raise_on_error)
 
 
 def dpp_cfg_workspace_bytes(n: int) -> int:

@@ -105,6 +105,12 @@ dpp_status check_attn(const dpp_attn_desc *d, bool cross) {
 
 size_t attn_tokens(const dpp_attn_desc &d) { return (size_t)d.B * d.H * d.W; }
 
+// Bytes of the context K/V [B, n_ctx, 2, C] in the attention state type.
+size_t ctx_kv_bytes(const dpp_attn_desc &d) {
+  return (size_t)d.B * d.n_ctx * 2 * d.C * elem_bytes(inter_elem(d.dtype));
+}
+
+
 std::atomic<uint64_t> g_launches{0};
 cudaEvent_t g_core_start = nullptr, g_core_stop = nullptr;
 
@@ -352,10 +358,8 @@ size_t dpp_self_attn_workspace_bytes(const dpp_attn_desc *d) {
 
 size_t dpp_cross_attn_workspace_bytes(const dpp_attn_desc *d) {
   if (check_attn(d, true) != DPP_OK) return 0;
-  const size_t es = elem_bytes(inter_elem(d->dtype));
-  const size_t n = attn_tokens(*d) * d->C * es;
-  const size_t kv = (size_t)d->B * d->n_ctx * 2 * d->C * es;
-  return 2 * align_up(n, 256) + align_up(kv, 256) + wo16_bytes(*d);  // Q, O, ctx K/V, Wo
+  // the cached call's Q, O and fp16 Wo, then the context K/V
+  return dpp_cross_attn_cached_workspace_bytes(d) + align_up(ctx_kv_bytes(*d), 256);
 }
 
 dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, const void *wk,
@@ -400,6 +404,68 @@ dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, 
   return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256), y, M, s));
 }
 
+dpp_status dpp_cross_attn_kv(const dpp_attn_desc *d, const void *ctx, const void *wk,
+                             const void *wv, void *kv_ctx, dpp_stream stream) {
+  dpp_status st = check_attn(d, true);
+  if (st != DPP_OK) return st;
+  if (!ctx || !wk || !wv || !kv_ctx) return DPP_ERR_INVALID_ARG;
+  const void *ptrs[] = {ctx, wk, wv, kv_ctx};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return DPP_ERR_ALIGN;
+  const size_t es = elem_size(d->dtype);
+  const size_t nkv = ctx_kv_bytes(*d);
+  if (overlap(kv_ctx, nkv, ctx, (size_t)d->B * d->n_ctx * d->c_ctx * es) ||
+      overlap(kv_ctx, nkv, wk, (size_t)d->C * d->c_ctx * es) ||
+      overlap(kv_ctx, nkv, wv, (size_t)d->C * d->c_ctx * es))
+    return DPP_ERR_ALIAS;
+  const Elem te = inter_elem(d->dtype), tl = layer_elem(d->dtype);
+  const int C = d->C;
+  GemmArgs kvg{ctx, {wk, wv, nullptr}, C, d->B * d->n_ctx, 2 * C, d->c_ctx,
+               kv_ctx, 2 * C, 2 * C, nullptr, 0, tl, tl, te};
+  return from_cuda(gemm(kvg, (cudaStream_t)stream));
+}
+
+size_t dpp_cross_attn_cached_workspace_bytes(const dpp_attn_desc *d) {
+  if (check_attn(d, true) != DPP_OK) return 0;
+  const size_t n = attn_tokens(*d) * d->C * elem_bytes(inter_elem(d->dtype));
+  return 2 * align_up(n, 256) + wo16_bytes(*d);  // Q, O, fp16 Wo
+}
+
+dpp_status dpp_cross_attn_cached(const dpp_attn_desc *d, const void *x, const void *kv_ctx,
+                                 const void *wq, const void *wo, void *y, void *ws,
+                                 size_t ws_bytes, dpp_stream stream) {
+  dpp_status st = check_attn(d, true);
+  if (st != DPP_OK) return st;
+  if (!x || !kv_ctx || !wq || !wo || !y) return DPP_ERR_INVALID_ARG;
+  const void *ptrs[] = {x, kv_ctx, wq, wo, y, ws};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return DPP_ERR_ALIGN;
+  const size_t need = dpp_cross_attn_cached_workspace_bytes(d);
+  if (!ws || ws_bytes < need) return DPP_ERR_WORKSPACE;
+  const size_t es = elem_size(d->dtype);
+  const Elem te = inter_elem(d->dtype), tl = layer_elem(d->dtype);
+  const size_t nt = attn_tokens(*d);
+  const size_t nx = nt * d->C * es;
+  const size_t nq = nt * d->C * elem_bytes(te);
+  const size_t nkv = ctx_kv_bytes(*d);
+  if (overlap(ws, need, y, nx) || overlap(ws, need, x, nx) || overlap(ws, need, kv_ctx, nkv) ||
+      overlap(y, nx, kv_ctx, nkv))
+    return DPP_ERR_ALIAS;
+  if (y != x && overlap(y, nx, x, nx)) return DPP_ERR_ALIAS;
+  cudaStream_t s = (cudaStream_t)stream;
+  char *wsb = reinterpret_cast<char *>(ws);
+  void *q = wsb;
+  void *o = wsb + align_up(nq, 256);
+  const int C = d->C;
+  GemmArgs qg{x, {wq, nullptr, nullptr}, C, (int)nt, C, C, q, C, C, nullptr, 0, tl, tl, te};
+  cudaError_t e = gemm(qg, s);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  AttnArgs a{q, kv_ctx, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, te, 0};
+  e = attn_core(a, s);
+  if (e != cudaSuccess) return DPP_ERR_CUDA;
+  return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256), y, (int)nt, s));
+}
+
 dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx, const void *wq,
                           const void *wk, const void *wv, const void *wo, void *y, void *ws,
                           size_t ws_bytes, dpp_stream stream) {
@@ -412,33 +478,19 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx
   const size_t need = dpp_cross_attn_workspace_bytes(d);
   if (!ws || ws_bytes < need) return DPP_ERR_WORKSPACE;
   const size_t es = elem_size(d->dtype);
-  const Elem te = inter_elem(d->dtype), tl = layer_elem(d->dtype);
   const size_t nt = attn_tokens(*d);
   const size_t nx = nt * d->C * es;
-  const size_t nq = nt * d->C * elem_bytes(te);
   if (overlap(ws, need, y, nx) || overlap(ws, need, x, nx) ||
       overlap(ws, need, ctx, (size_t)d->B * d->n_ctx * d->c_ctx * es))
     return DPP_ERR_ALIAS;
   if (y != x && overlap(y, nx, x, nx)) return DPP_ERR_ALIAS;
-  cudaStream_t s = (cudaStream_t)stream;
+  // the context K/V in the workspace after the cached call's Q, O and Wo
   char *wsb = reinterpret_cast<char *>(ws);
-  void *q = wsb;
-  void *o = wsb + align_up(nq, 256);
-  void *kv = wsb + 2 * align_up(nq, 256);
-  const int C = d->C;
-  GemmArgs qg{x, {wq, nullptr, nullptr}, C, (int)nt, C, C, q, C, C, nullptr, 0, tl, tl, te};
-  cudaError_t e = gemm(qg, s);
-  if (e != cudaSuccess) return DPP_ERR_CUDA;
-  GemmArgs kvg{ctx, {wk, wv, nullptr}, C, d->B * d->n_ctx, 2 * C, d->c_ctx,
-               kv, 2 * C, 2 * C, nullptr, 0, tl, tl, te};
-  e = gemm(kvg, s);
-  if (e != cudaSuccess) return DPP_ERR_CUDA;
-  AttnArgs a{q, kv, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, te, 0};
-  e = attn_core(a, s);
-  if (e != cudaSuccess) return DPP_ERR_CUDA;
-  const size_t nkvb = (size_t)d->B * d->n_ctx * 2 * d->C * elem_bytes(te);
-  return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256) + align_up(nkvb, 256), y,
-                            (int)nt, s));
+  const size_t cached = dpp_cross_attn_cached_workspace_bytes(d);
+  void *kv = wsb + cached;
+  st = dpp_cross_attn_kv(d, ctx, wk, wv, kv, stream);
+  if (st != DPP_OK) return st;
+  return dpp_cross_attn_cached(d, x, kv, wq, wo, y, ws, cached, stream);
 }
 
 dpp_status dpp_wait_selftest(int kind, void *scratch, dpp_stream stream) {

@@ -305,6 +305,28 @@ dpp_status dpp_cross_attn(const dpp_attn_desc *desc, const void *x, const void *
 size_t dpp_cross_attn_workspace_bytes(const dpp_attn_desc *desc);
 
 /* ---------------------------------------------------------------------------
+ * dpp_cross_attn_kv + dpp_cross_attn_cached -- dpp_cross_attn in two parts,
+ * so that the context's K and V are projected once per prompt (the text
+ * context is the same at every denoising step) instead of once per call:
+ *   dpp_cross_attn_kv:     kv_ctx[b, t, 0, :] = ctx[b, t] wk^T,
+ *                          kv_ctx[b, t, 1, :] = ctx[b, t] wv^T.
+ *   dpp_cross_attn_cached: y = softmax((x wq^T) K^T / sqrt(head_dim)) V wo^T
+ *                          with K, V from kv_ctx.
+ *   kv_ctx : [B, n_ctx, 2, C] (K then V per context token), fp16 for
+ *            DPP_BF16 layers, fp32 for DPP_F32 layers; written by
+ *            dpp_cross_attn_kv, read by dpp_cross_attn_cached.
+ *   ws     : dpp_cross_attn_cached_workspace_bytes(desc) bytes (Q and O).
+ * The pair computes exactly what dpp_cross_attn computes (same kernels in
+ * the same order), which is itself the two calls back to back.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_cross_attn_kv(const dpp_attn_desc *desc, const void *ctx, const void *wk,
+                             const void *wv, void *kv_ctx, dpp_stream stream);
+dpp_status dpp_cross_attn_cached(const dpp_attn_desc *desc, const void *x, const void *kv_ctx,
+                                 const void *wq, const void *wo, void *y, void *ws,
+                                 size_t ws_bytes, dpp_stream stream);
+size_t dpp_cross_attn_cached_workspace_bytes(const dpp_attn_desc *desc);
+
+/* ---------------------------------------------------------------------------
  * dpp_cfg_combine -- classifier-free-guidance combine and the denoising
  * discrepancy of the Hydiff summaries (gist.science, "基于条件的数据划分"
  * and "自适应并行切换"; Avetisyan, "Адаптивное переключение"):

@@ -346,3 +346,17 @@ def test_library_is_built_from_these_sources():
     assert dpp.dpp_source_hash() == b.source_hash()
     assert b.library_hash() == b.source_hash()
     assert b.library_hash(os.path.join(ROOT, "no_such_library.so")) is None
+
+
+def test_cached_cross_attention_arguments_checked_on_the_host():
+    d = dpp.dpp_attn_desc(1, 4, 4, 64, 1, 64, 1, 77, 96, dpp.DPP_BF16, 0, 0)
+    before = dpp.dpp_launch_count()
+    st = dpp.dpp_cross_attn_kv(d, A, Bp, Cp, None, stream=0, raise_on_error=False)
+    assert st == dpp.DPP_ERR_INVALID_ARG
+    st = dpp.dpp_cross_attn_kv(d, A + 8, Bp, Cp, Dp, stream=0, raise_on_error=False)
+    assert st == dpp.DPP_ERR_ALIGN
+    n = dpp.dpp_cross_attn_cached_workspace_bytes(d)
+    assert n > 0
+    st = dpp.dpp_cross_attn_cached(d, A, Bp, Cp, Dp, Ep, None, 0, stream=0, raise_on_error=False)
+    assert st == dpp.DPP_ERR_WORKSPACE
+    assert dpp.dpp_launch_count() == before

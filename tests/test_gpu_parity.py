@@ -289,6 +289,36 @@ def test_cross_attn_matches_oracle(cuda_device, B, H, W, heads, n_ctx, c_ctx, dt
     G.assert_rms_close(G.f64(y), ref, G.TOL[dt], "cross-attn")
 
 
+@pytest.mark.parametrize("dt", [BF16, F32])
+def test_cross_attn_context_kv_once_per_prompt(cuda_device, dt):
+    """The context's K/V projected once (dpp_cross_attn_kv) and reused by
+    dpp_cross_attn_cached over several calls: bit-identical to
+    dpp_cross_attn, which is the two parts back to back, and to the oracle
+    within the bar."""
+    B, H, W, heads, n_ctx, c_ctx = 2, 8, 12, 2, 77, 96
+    N, C = H * W, 64 * heads
+    a = wl.AttnShape(B, H, W, C, heads, 64, 1, n_ctx, c_ctx)
+    name = "bf16" if dt == BF16 else "f32"
+    ctx = G.cuda(wl.normal((B, n_ctx, c_ctx), 511, dtype=name))
+    w = {k: G.cuda(v) for k, v in wl.cross_weights(a, 7, name).items()}
+    d = G.dpp.dpp_attn_desc(B, H, W, C, heads, 64, 1, n_ctx, c_ctx, G.CODES[dt], 0, 0)
+    kv = torch.empty((B, n_ctx, 2, C), dtype=G.KV_DTYPE[dt], device="cuda")
+    G.dpp.dpp_cross_attn_kv(d, ctx, w["wk"], w["wv"], kv)
+    nws = G.dpp.dpp_cross_attn_cached_workspace_bytes(d)
+    assert 0 < nws < G.dpp.dpp_cross_attn_workspace_bytes(d)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    w64 = {k: G.f64(v) for k, v in w.items()}
+    for step in range(3):  # one prompt, several denoising steps
+        X = G.cuda(draw((B, N, C), 520 + step, dt))
+        y = torch.empty_like(X)
+        G.dpp.dpp_cross_attn_cached(d, X, kv, w["wq"], w["wo"], y, ws, nws)
+        y_full = G.cross_attn(X, ctx, {k: v for k, v in w.items()}, H, W, heads)
+        assert torch.equal(y, y_full)
+        ref = oracle.cross_attention(G.f64(X), G.f64(ctx), w64["wq"], w64["wk"], w64["wv"],
+                                     w64["wo"], heads)
+        G.assert_rms_close(G.f64(y), ref, G.TOL[dt], "cross-attn, cached context K/V")
+
+
 def test_bf16_attention_reports_fp16_range(cuda_device):
     """A bf16 attention layer holds Q, K and V in fp16.  Inputs large enough
     that a projected K exceeds 65504 are reported as DPP_ERR_RANGE in the
