@@ -7,18 +7,25 @@
 // refresh of DistriSelfAttentionPP's state costs no extra pass).
 //
 // Persistent, warp-specialised, one CTA per SM:
-//   warp 0      TMA producer (the warp stays converged; an elected lane issues
-//               each copy): A tile 128 x 64 and B tile BN x 64 per stage
-//               (B as BN/64 boxes of 64 rows, each from the weight block that
-//               holds it), 128-byte swizzle, STAGES-deep mbarrier ring;
+//   warp 0      TMA producer (converged warp, an elected lane issues each
+//               copy): per stage the A tile 128 x 64 and the B tile BN x 64
+//               as ONE box each (column tiles never straddle two weight
+//               blocks, so a tile's B rows are one box of one block),
+//               128-byte swizzle, STAGES-deep mbarrier ring.  Few large
+//               copies matter: a thread that issues bulk tensor copies pays
+//               a fixed cost per copy, and four 64-row boxes per stage fed
+//               the tensor pipe at under half its rate;
 //   warp 1      TMEM allocation and the tcgen05.mma issuer (converged warp,
-//               one elected lane per instruction)
-//               (M = 128, N = BN, K = 16 per instruction), fp32 accumulators
+//               one elected lane per instruction), M = 128, N = the tile's
+//               width, K = 16 per instruction, fp32 accumulators
 //               double-buffered in TMEM (2 x BN columns);
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, + bias (a per-warp
-//               shared-memory copy of the tile's), + the residual in out0
-//               (prefetched before the accumulator is ready), convert, store;
-//               or the gated-GELU epilogue (value * GELU(gate)).
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant, each converting
+//               half of the tile's columns: tcgen05.ld 32 columns at a time
+//               (the next chunk's load in flight while one is converted),
+//               + bias (broadcast 16-byte loads), + the residual already in
+//               out0 (loaded a chunk ahead), convert, stage in shared memory
+//               (64-byte swizzle: conflict-free), one bulk tensor store per
+//               32 x 32 chunk; or the gated-GELU epilogue (value * GELU(gate)).
 // Tiles are ordered n-fastest so CTAs running together share A rows in L2.
 #include "tc_common.cuh"
 
@@ -66,31 +73,59 @@ struct GemmTcParams {
   int ld1;
   int out_f16;  // 1: fp16 output, 0: bf16 output
   int m_tiles, n_tiles;
+  int tpb;      // column tiles per weight block (plain GEMM)
   int *status;
   const float *bias;  // per out0 column ([2 N] with geglu: value then gate), or null
   int accumulate;     // out0 += result
   int geglu;          // tile = BN/2 value rows of B0 + BN/2 gate rows of B1
+  int pf_boxes;       // residual L2 prefetch boxes per tile (0: no residual)
+  int pf_cols;        // columns per prefetch box
 };
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int BM = 128, BK = 64;
+constexpr uint32_t kStageOut = 2048;  // one 32 x 32 chunk of 16-bit outputs
+
+// Columns of column tile j: output columns [n0, n0 + w) from weight block
+// `mat`, rows [brow, brow + w) of it.  A plain GEMM tiles each weight block
+// on its own (tiles of BN, the last one narrower); gated GELU tiles the N
+// output columns by BN/2 (value and gate rows of the same columns).
+template <int BN>
+__device__ __forceinline__ bool tile_cols(const GemmTcParams &p, int j, int &n0, int &w, int &mat,
+                                          int &brow) {
+  if (p.geglu) {
+    n0 = j * (BN / 2);
+    w = min(BN / 2, p.N - n0);
+    mat = 0;
+    brow = n0;
+  } else {
+    const int blk = j / p.tpb, off = (j % p.tpb) * BN;
+    n0 = blk * p.b_rows + off;
+    w = min(min(BN, p.b_rows - off), p.N - n0);
+    mat = blk;
+    brow = off;
+  }
+  return w > 0;
+}
 
 template <int BN, int STAGES, bool IN_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
-               const GemmTcParams p) {
+               const __grid_constant__ CUtensorMap tmR, const GemmTcParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
-  constexpr uint32_t IDESC = idesc_f16(BM, BN, IN_BF16);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  // per epilogue warp two output staging buffers, then the barriers
+  uint8_t *stage_out = smem + STAGES * STAGE_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(stage_out + kEpiWarps * 2 * kStageOut);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
@@ -106,7 +141,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty[a], kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -121,6 +156,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     prefetch_tmap(&tmB0);
     prefetch_tmap(&tmB1);
     prefetch_tmap(&tmB2);
+    if (p.pf_boxes) prefetch_tmap(&tmR);
   }
   tc_fence_before();
   __syncthreads();
@@ -135,33 +171,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;  // per-stage bits, for the abort drain
       for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-        const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
-        // 64-row boxes of B this tile needs (a ragged last tile of a plain
-        // GEMM loads, and multiplies, only its own columns)
-        const int nbox = p.geglu ? BN / 64 : min(BN / 64, (p.N - n0 + 63) / 64);
+        int n0, w, mat, brow;
+        if (!tile_cols<BN>(p, t % p.n_tiles, n0, w, mat, brow)) continue;
+        const int m0 = (t / p.n_tiles) * BM;
+        const CUtensorMap *mb = mat == 0 ? &tmB0 : (mat == 1 ? &tmB1 : &tmB2);
+        // The residual the epilogue adds is pulled into L2 now, a whole tile
+        // of MMAs before it is read: per-thread loads issued only a chunk
+        // ahead cannot keep enough bytes in flight to cover DRAM latency.
+        if (p.pf_boxes && n0 < p.split)
+          for (int b = 0; b < p.pf_boxes && b * p.pf_cols < w; ++b)
+            tma_prefetch_l2_2d_w(&tmR, n0 + b * p.pf_cols, m0);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
           uint8_t *sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx_w(&full[stage], A_BYTES + nbox * 64 * BK * 2);
+          // full boxes are always credited (rows outside a block read as zero)
+          mbar_arrive_expect_tx_w(&full[stage], STAGE_BYTES);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           tma_load_2d_w(sa, &tmA, &full[stage], kb * BK, m0);
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j) {
-            if (j >= nbox) break;
-            if (p.geglu) {  // value rows, then the matching gate rows
-              const bool gate = j >= BN / 128;
-              const int n = n0 / 2 + 64 * (gate ? j - BN / 128 : j);
-              tma_load_2d_w(sa + A_BYTES + j * 64 * 128, gate ? &tmB1 : &tmB0, &full[stage],
-                          kb * BK, n);
-              continue;
-            }
-            const int n = n0 + 64 * j;
-            int mat = n / p.b_rows;
-            if (mat > 2) mat = 2;
-            const CUtensorMap *mp = mat == 0 ? &tmB0 : (mat == 1 ? &tmB1 : &tmB2);
-            tma_load_2d_w(sa + A_BYTES + j * 64 * 128, mp, &full[stage], kb * BK,
-                        n - mat * p.b_rows);
+          if (p.geglu) {  // value rows, then the gate rows of the same columns
+            tma_load_2d_w(sa + A_BYTES, &tmB0, &full[stage], kb * BK, brow);
+            tma_load_2d_w(sa + A_BYTES + (BN / 2) * 128, &tmB1, &full[stage], kb * BK, brow);
+          } else {
+            tma_load_2d_w(sa + A_BYTES, mb, &full[stage], kb * BK, brow);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -178,15 +210,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        int n0, w, mat, brow;
+        if (!tile_cols<BN>(p, t % p.n_tiles, n0, w, mat, brow)) continue;
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
+        ++it;
         if (!mbar_wait_w(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
-        const int n0 = (t % p.n_tiles) * BN;
-        const uint32_t idesc =
-            p.geglu ? IDESC : idesc_f16(BM, 64 * min(BN / 64, (p.N - n0 + 63) / 64), IN_BF16);
+        // a narrow last tile multiplies only its own columns
+        const uint32_t idesc = idesc_f16(BM, p.geglu ? BN : ((w + 15) & ~15), IN_BF16);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_w(&full[stage], phase, abort_flag, p.status)) {
@@ -215,72 +249,58 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
   } else {  // ------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;         // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) / 4;  // which half of the tile's columns it converts
     const int row = q * 32 + lane;
-    // this warp's copy of the tile's bias (gated GELU: value bias, then gate bias)
-    float *bias_s = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES + 512) + q * BN;
-    // this warp's two output staging buffers (32 rows x 32 columns of 16-bit
-    // values each) for the bulk tensor stores
-    uint8_t *stage_o = smem + STAGES * STAGE_BYTES + 512 + 4 * BN * sizeof(float) + q * 4096;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    // this warp's two output staging buffers (32 rows x 64 bytes each,
+    // 16-byte units swizzled by the row as the 64-byte tensor-map swizzle does)
+    uint8_t *stage_o = stage_out + (warp - 2) * 2 * kStageOut;
     int n_stored = 0;  // chunks this warp has handed to the bulk-store engine
-    constexpr int PRE = BN <= 128 ? BN / 8 : 1;  // residual vectors a thread prefetches
     int it = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      int n0, w, mat, brow;
+      if (!tile_cols<BN>(p, t % p.n_tiles, n0, w, mat, brow)) continue;
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      const int m0 = (t / p.n_tiles) * BM, n0 = (t % p.n_tiles) * BN;
+      ++it;
+      const int m0 = (t / p.n_tiles) * BM;
       const int m = m0 + row;
-      // Before the accumulator is ready, so that neither latency lands after
-      // the MMA: the tile's bias into this warp's slice, and (128-column
-      // tiles) the loads of the residual row already in out0.
-      if (p.bias) {
-        __syncwarp();  // this warp's reads of the previous tile's slice are done
-        for (int j = lane; j < BN; j += 32) {
-          float b = 0.f;
-          if (p.geglu) {
-            const int jj = j < BN / 2 ? j : j - BN / 2;
-            if (n0 / 2 + jj < p.N) b = __ldg(p.bias + (j < BN / 2 ? 0 : p.N) + n0 / 2 + jj);
-          } else if (n0 + j < p.N && n0 + j < p.split) {
-            b = __ldg(p.bias + n0 + j);
-          }
-          bias_s[j] = b;
-        }
-        __syncwarp();
-      }
-      uint4 pre[PRE];
-      if constexpr (BN <= 128) {
-        const bool pre_acc = p.accumulate && !p.geglu && m < p.M;
-#pragma unroll
-        for (int k = 0; k < PRE; ++k) {
-          const int n = n0 + 8 * k;
-          pre[k] = pre_acc && n < p.N && n < p.split
-                       ? *reinterpret_cast<const uint4 *>(
-                             reinterpret_cast<const uint16_t *>(p.out0) + (size_t)m * p.ld0 + n)
-                       : make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
       // every lane leaves together (a lane that timed out has set the abort flag)
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)))
         break;
       tc_fence_after();
       if (p.geglu) {
-        // value columns [0, BN/2) and gate columns [BN/2, BN) of the tile:
-        // out[n0/2 + j] = (value_j + b_j) * GELU(gate_j + b_{N + j})
+        // value columns [0, BN/2) and gate columns [BN/2, BN) of the
+        // accumulator: out[n0 + j] = (value_j + b_j) * GELU(gate_j + b_{N + j})
+        constexpr int CH = BN / 128;  // value chunks per warp
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int cc = 0; cc < CH; ++cc) {
+          const int c = half * CH + cc;
+          if (c * 32 >= w) break;  // warp-uniform
           uint32_t rv[32], rg[32];
-          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32;
+          const uint32_t ta = tq + acc * BN + c * 32;
           tmem_ld32(ta, rv);
           tmem_ld32(ta + BN / 2, rg);
-          const int n = n0 / 2 + c * 32;
+          const int n = n0 + c * 32;
           __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out0) + (size_t)m * p.ld0 + n;
-          const bool in = m < p.M && n < p.N;
+          const bool in = m < p.M;
           uint4 res[4];  // loads in flight while the accumulator is read
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             res[v] = in && p.accumulate ? reinterpret_cast<const uint4 *>(dst)[v]
                                         : make_uint4(0u, 0u, 0u, 0u);
+          float4 bv[8], bg[8];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            bv[v] = p.bias ? __ldg(reinterpret_cast<const float4 *>(p.bias + n) + v)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            bg[v] = p.bias ? __ldg(reinterpret_cast<const float4 *>(p.bias + p.N + n) + v)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
           tmem_wait_ld();
+          const float *bvf = reinterpret_cast<const float *>(bv);
+          const float *bgf = reinterpret_cast<const float *>(bg);
           if (in) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -293,9 +313,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int k = v * 8 + 2 * e + h;
-                  const float a = __uint_as_float(rv[k]) + (p.bias ? bias_s[c * 32 + k] : 0.f);
-                  const float g =
-                      __uint_as_float(rg[k]) + (p.bias ? bias_s[BN / 2 + c * 32 + k] : 0.f);
+                  const float a = __uint_as_float(rv[k]) + bvf[k];
+                  const float g = __uint_as_float(rg[k]) + bgf[k];
                   f[h] = a * (0.5f * g * (1.f + erff(g * 0.70710678118654752f)));
                 }
                 f[0] += __uint_as_float(rw[e] << 16);
@@ -312,80 +331,84 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         continue;
       }
       float amax = 0.f;  // largest |value| this thread stores (fp16 range check)
-      // Each 32 x 32 chunk is converted into a staging buffer (row = lane,
-      // 64 bytes) and written by one bulk tensor store: whole cache lines,
-      // asynchronous, rows past M clipped by the tensor map.  With a
-      // residual to add, the next chunk's residual loads are issued before
-      // this chunk is converted, so their latency overlaps the work.
+      constexpr int CH = BN / 64;  // 32-column chunks per warp
+      const int c_begin = half * CH;
+      const int c_end = min(c_begin + CH, (w + 31) / 32);
+      // Each 32 x 32 chunk is converted into a staging buffer and written by
+      // one bulk tensor store: whole cache lines, asynchronous, rows past M
+      // clipped by the tensor map.  The residual is loaded a chunk ahead,
+      // and the next chunk's accumulator columns are read while this one is
+      // converted; the bias is a broadcast load that hits L1.
       auto residual = [&](int c, uint4 (&rr)[4]) {
         const int n = n0 + c * 32;
-        const bool ld = p.accumulate && m < p.M && n < p.N && n < p.split;
+        const bool ld = p.accumulate && n < p.split && m < p.M;
 #pragma unroll
         for (int v = 0; v < 4; ++v)
           rr[v] = ld ? reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.out0) +
                                                        (size_t)m * p.ld0 + n)[v]
                      : make_uint4(0u, 0u, 0u, 0u);
       };
-      uint4 res_next[4];
-      if constexpr (BN > 128) residual(0, res_next);
+      if (c_begin < c_end) {
+        uint4 res_next[4];
+        residual(c_begin, res_next);
+        uint32_t rr2[2][32];
+        tmem_ld32(tq + acc * BN + c_begin * 32, rr2[0]);
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c * 32, r);
-        const int n = n0 + c * 32;
-        const bool col_in = n < p.N;
-        const bool first = n < p.split;
-        const bool acc_in = first && p.accumulate;
-        uint4 res[4];  // the residual already in out0
-        if constexpr (BN <= 128) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) res[v] = pre[c * 4 + v];
-        } else {
+        for (int cc = 0; cc < CH; ++cc) {
+          const int c = c_begin + cc;
+          if (c >= c_end) break;  // warp-uniform
+          uint32_t(&r)[32] = rr2[cc & 1];
+          const int n = n0 + c * 32;
+          const bool first = n < p.split;
+          const bool acc_in = first && p.accumulate;
+          uint4 res[4];
 #pragma unroll
           for (int v = 0; v < 4; ++v) res[v] = res_next[v];
-          if (c + 1 < BN / 32) residual(c + 1, res_next);
-        }
-        tmem_wait_ld();
-        if (!col_in) continue;  // warp-uniform: the whole chunk lies past N
-        uint8_t *buf = stage_o + (n_stored & 1) * 2048;
-        if (n_stored >= 2) {  // the store that read this buffer two chunks ago
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-        }
+          if (c + 1 < c_end) residual(c + 1, res_next);
+          tmem_wait_ld();
+          if (cc + 1 < CH && c + 1 < c_end) tmem_ld32(tq + acc * BN + (c + 1) * 32, rr2[(cc + 1) & 1]);
+          float4 bias4[8];  // the chunk's bias, zero outside out0's columns
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 o;
-          uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
-          const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = v * 8 + 2 * e;
-            float a = __uint_as_float(r[k]);
-            float b = __uint_as_float(r[k + 1]);
-            if (p.bias) {  // zero outside out0's columns
-              a += bias_s[c * 32 + k];
-              b += bias_s[c * 32 + k + 1];
-            }
-            if (acc_in) {  // out0 is bf16 or fp16, as the output
-              if (p.out_f16) {
-                const float2 old = __half22float2(*reinterpret_cast<const __half2 *>(&rw[e]));
-                a += old.x;
-                b += old.y;
-              } else {
-                a += __uint_as_float(rw[e] << 16);
-                b += __uint_as_float(rw[e] & 0xffff0000u);
-              }
-            }
-            if (p.out_f16) amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
-            ow[e] = p.out_f16 ? pack_half2(a, b) : pack_bf162(a, b);
+          for (int v = 0; v < 8; ++v)
+            bias4[v] = p.bias && first ? __ldg(reinterpret_cast<const float4 *>(p.bias + n) + v)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float *bf = reinterpret_cast<const float *>(bias4);
+          uint8_t *buf = stage_o + (n_stored & 1) * kStageOut;
+          if (n_stored >= 2) {  // the store that read this buffer two chunks ago
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
           }
-          *reinterpret_cast<uint4 *>(buf + lane * 64 + v * 16) = o;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+            const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = v * 8 + 2 * e;
+              float a = __uint_as_float(r[k]) + bf[k];
+              float b = __uint_as_float(r[k + 1]) + bf[k + 1];
+              if (acc_in) {  // out0 is bf16 or fp16, as the output
+                if (p.out_f16) {
+                  const float2 old = __half22float2(*reinterpret_cast<const __half2 *>(&rw[e]));
+                  a += old.x;
+                  b += old.y;
+                } else {
+                  a += __uint_as_float(rw[e] << 16);
+                  b += __uint_as_float(rw[e] & 0xffff0000u);
+                }
+              }
+              if (p.out_f16) amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+              ow[e] = p.out_f16 ? pack_half2(a, b) : pack_bf162(a, b);
+            }
+            *reinterpret_cast<uint4 *>(buf + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = o;
+          }
+          fence_proxy_async_smem();  // the generic-proxy writes, before the bulk copy reads them
+          __syncwarp();
+          if (lane == 0)  // lane 0 issues, and later waits for, this warp's stores
+            tma_store_2d(first ? &tmO0 : &tmO1, buf, first ? n : n - p.split, m0 + q * 32);
+          ++n_stored;
         }
-        fence_proxy_async_smem();  // the generic-proxy writes, before the bulk copy reads them
-        __syncwarp();
-        if (lane == 0)  // lane 0 issues, and later waits for, this warp's stores
-          tma_store_2d(first ? &tmO0 : &tmO1, buf, first ? n : n - p.split, m0 + q * 32);
-        ++n_stored;
       }
       // An fp16 output (the attention state of a bf16 layer) cannot hold a
       // value above 65504: such a call is reported, not silently saturated.
@@ -418,16 +441,18 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
     if (!encode_tiled(&ma, ty, 2, g.A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  // one box per weight block and stage: BN rows (gated GELU: BN/2 value rows
+  // and BN/2 gate rows)
   for (int i = 0; i < 3; ++i) {
     const void *b = g.B[i] ? g.B[i] : g.B[0];
     const uint64_t dims[2] = {(uint64_t)g.K, (uint64_t)g.b_rows};
     const uint64_t str[1] = {(uint64_t)g.K * 2};
-    const uint32_t box[2] = {64, 64};
+    const uint32_t box[2] = {64, (uint32_t)(g.geglu ? BN / 2 : BN)};
     if (!encode_tiled(&mb[i], ty, 2, b, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  // output tensor maps (16-bit, 32 x 32 boxes, no swizzle): out0 holds columns
-  // [0, split) (all N without a second destination), out1 columns [split, N)
+  // output tensor maps (16-bit, 32 x 32 boxes, 64-byte swizzle): out0 holds
+  // columns [0, split) (all N without a second destination), out1 [split, N)
   CUtensorMap mo[2];
   {
     const CUtensorMapDataType to = tma_type(g.to);
@@ -435,24 +460,48 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
     const uint64_t d0[2] = {(uint64_t)w0, (uint64_t)g.M};
     const uint64_t s0[1] = {(uint64_t)g.ld0 * 2};
     const uint32_t box[2] = {32, 32};
-    if (!encode_tiled(&mo[0], to, 2, g.out0, d0, s0, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_tiled(&mo[0], to, 2, g.out0, d0, s0, box, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
     mo[1] = mo[0];
     if (g.out1 && g.N > g.split) {
       const uint64_t d1[2] = {(uint64_t)(g.N - g.split), (uint64_t)g.M};
       const uint64_t s1[1] = {(uint64_t)g.ld1 * 2};
-      if (!encode_tiled(&mo[1], to, 2, g.out1, d1, s1, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      if (!encode_tiled(&mo[1], to, 2, g.out1, d1, s1, box, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     }
   }
-  const int n_cols = g.geglu ? 2 * g.N : g.N;  // accumulator columns in all
+  // residual prefetch map over out0: one box of the tile's columns x 128
+  // rows (64-column boxes if the wide box cannot be encoded)
+  CUtensorMap mr = mo[0];
+  int pf_boxes = 0, pf_cols = 0;
+  if (g.accumulate) {
+    const CUtensorMapDataType to = tma_type(g.to);
+    const int w0 = g.out1 ? g.split : g.N;
+    const uint64_t d0[2] = {(uint64_t)w0, (uint64_t)g.M};
+    const uint64_t s0[1] = {(uint64_t)g.ld0 * 2};
+    const uint32_t cols = g.geglu ? BN / 2 : BN;
+    const uint32_t box[2] = {cols, 128};
+    if (encode_tiled(&mr, to, 2, g.out0, d0, s0, box, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      pf_boxes = 1;
+      pf_cols = (int)cols;
+    } else {
+      const uint32_t box64[2] = {64, 128};
+      if (!encode_tiled(&mr, to, 2, g.out0, d0, s0, box64, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+      pf_boxes = (int)cols / 64;
+      pf_cols = 64;
+    }
+  }
+  const int tpb = (g.b_rows + BN - 1) / BN;
+  const int n_tiles = g.geglu ? (g.N + BN / 2 - 1) / (BN / 2)
+                              : ((g.N + g.b_rows - 1) / g.b_rows) * tpb;
   GemmTcParams p{g.M, g.N, g.K, g.b_rows, g.out0, g.ld0, g.split, g.out1, g.ld1,
-                 g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, (n_cols + BN - 1) / BN, status,
-                 g.bias, g.accumulate ? 1 : 0, g.geglu ? 1 : 0};
-  // stages, 1024-byte alignment slack, barriers, the epilogue warps' bias
-  // slices and output staging buffers
-  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 512 +
-                          4 * BN * sizeof(float) + 4 * 4096;
+                 g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, n_tiles, tpb, status,
+                 g.bias, g.accumulate ? 1 : 0, g.geglu ? 1 : 0, pf_boxes, pf_cols};
+  // stages, 1024-byte alignment slack, the epilogue warps' staging buffers, barriers
+  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 +
+                          (size_t)kEpiWarps * 2 * kStageOut + 256;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
   auto k = gemm_tc_kernel<BN, STAGES, IN_BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -461,7 +510,7 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = p.m_tiles * p.n_tiles;
   const int grid = tiles < sms ? tiles : sms;
-  k<<<grid, kThreads, smem, s>>>(ma, mb[0], mb[1], mb[2], mo[0], mo[1], p);
+  k<<<grid, kThreads, smem, s>>>(ma, mb[0], mb[1], mb[2], mo[0], mo[1], mr, p);
   return cudaGetLastError();
 }
 
@@ -510,6 +559,7 @@ cudaError_t launch_cast_bf16_f16(const void *in, void *out, size_t n, cudaStream
 bool gemm_tc_supported(const GemmArgs &g) {
   const bool in16 = (g.ta == E_BF16 || g.ta == E_F16) && g.ta == g.tb;
   const bool out16 = g.to == E_BF16 || g.to == E_F16;
+  if (g.bias && (reinterpret_cast<uintptr_t>(g.bias) & 15u)) return false;  // float4 loads
   if (g.geglu)  // value / gate blocks of N rows; bf16 output; tiles of 64 or 128 columns
     return in16 && g.to == E_BF16 && g.K % 8 == 0 && g.N % 64 == 0 && g.b_rows == g.N &&
            g.split == g.N && g.out1 == nullptr && g.ld0 % 8 == 0 && g.M > 0 && g.B[1];

@@ -283,6 +283,17 @@ __device__ __forceinline__ void tma_load_4d_w(void *dst, const CUtensorMap *map,
       : "memory");
 }
 
+// L2 prefetch of one 2-D box (no shared memory, no completion to wait for),
+// issued by one elected lane of a converged warp.
+__device__ __forceinline__ void tma_prefetch_l2_2d_w(const CUtensorMap *map, int c0, int c1) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n\t}" ::"l"(map),
+      "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // Shared -> global tiled bulk store (2-D) by the calling thread, committed
 // as a bulk async-group of that thread (wait for it with bulk_wait_read /
 // bulk_wait_all from the same thread).  Elements outside the tensor map's
