@@ -155,8 +155,9 @@ cudaError_t out_proj(const dpp_attn_desc &d, const void *o, const void *wo, void
 // Launches the attention core, bracketed by the profiling events when set.
 cudaError_t attn_core(const AttnArgs &a, cudaStream_t s) {
   if (g_core_start && g_core_stop) cudaEventRecord(g_core_start, s);
-  cudaError_t e = attn_tc_supported(a) ? counted(launch_attn_tc(a, device_status_ptr(), s), 1)
-                                       : counted(launch_attn_simt(a, s), 1);
+  cudaError_t e = xattn_tc_supported(a)  ? counted(launch_xattn_tc(a, device_status_ptr(), s), 1)
+                  : attn_tc_supported(a) ? counted(launch_attn_tc(a, device_status_ptr(), s), 1)
+                                         : counted(launch_attn_simt(a, s), 1);
   if (g_core_start && g_core_stop) cudaEventRecord(g_core_stop, s);
   return e;
 }

@@ -119,6 +119,10 @@ struct AttnArgs {
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s);
 bool attn_tc_supported(const AttnArgs &a);
+// persistent core for keys that fit one tile (<= 128) without stale bands:
+// cross-attention over the text context
+cudaError_t launch_xattn_tc(const AttnArgs &a, int *status, cudaStream_t s);
+bool xattn_tc_supported(const AttnArgs &a);
 
 // token-wise LayerNorm (C <= 256 16-byte vectors)
 cudaError_t launch_layernorm(const dpp_ln_desc &d, const void *x, const float *gamma,

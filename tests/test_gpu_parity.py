@@ -289,6 +289,31 @@ def test_cross_attn_matches_oracle(cuda_device, B, H, W, heads, n_ctx, c_ctx, dt
     G.assert_rms_close(G.f64(y), ref, G.TOL[dt], "cross-attn")
 
 
+@pytest.mark.parametrize("B,H,W,heads,n_ctx", [
+    (2, 10, 30, 2, 1), (2, 10, 30, 2, 16), (2, 10, 30, 2, 17), (1, 10, 30, 2, 128),
+    (2, 64, 80, 3, 77)])
+def test_cross_attn_short_context_edges(cuda_device, B, H, W, heads, n_ctx):
+    """The persistent core for keys that fit one tile: a single key, exact
+    multiples of 16, one past, a full 128-key tile, query counts with a
+    ragged last tile per image (stores clipped at each image's end), and
+    more (image, head, query tile) items than SMs, so that a CTA walks
+    several items and changes head and image on the way.  A softmax over a
+    few keys is peaky, so the largest outputs sit far above the RMS: the bar
+    is 2e-2 x RMS on top of the bf16 storage floor (half an ulp of the
+    largest value), as for the chain's ops.  The tile-per-band core gives the
+    same errors on these inputs."""
+    N, C, c_ctx = H * W, 64 * heads, 96
+    a = wl.AttnShape(B, H, W, C, heads, 64, 1, n_ctx, c_ctx)
+    X = draw((B, N, C), 530, BF16)
+    ctx = wl.normal((B, n_ctx, c_ctx), 531, dtype="bf16")
+    wts = wl.cross_weights(a, 8, "bf16")
+    y = G.cross_attn(X, ctx, wts, H, W, heads)
+    w64 = {k: G.f64(v) for k, v in wts.items()}
+    ref = oracle.cross_attention(G.f64(X), G.f64(ctx), w64["wq"], w64["wk"], w64["wv"],
+                                 w64["wo"], heads)
+    G.assert_close_over_bf16_floor(G.f64(y), ref, G.TOL[BF16], "cross-attn, short context")
+
+
 @pytest.mark.parametrize("dt", [BF16, F32])
 def test_cross_attn_context_kv_once_per_prompt(cuda_device, dt):
     """The context's K/V projected once (dpp_cross_attn_kv) and reused by
