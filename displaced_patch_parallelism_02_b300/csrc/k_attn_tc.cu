@@ -6,8 +6,11 @@
 // O = softmax(Q K^T / 8) V per (batch, head, band), head_dim 64, fp16 Q/K/V/P,
 // fp32 accumulators and softmax.  One CTA handles two 128-query tiles of one
 // band so that one tile's softmax overlaps the other tile's MMAs:
-//   warp 0        TMA producer (converged warp, elected lane): both Q tiles once, then K and V tiles of 128
-//                 keys into 4-deep rings (128-byte swizzle).  The key range is
+//   warp 0        TMA producer (converged warp, elected lane): both Q tiles once, then
+//                 per tile of 128 keys ONE box of the K/V state viewed as
+//                 {channel, token, K or V}, landing as the K tile followed by
+//                 the V tile, into a 5-deep ring (128-byte swizzle): one copy
+//                 and one barrier pair per key tile.  The key range is
 //                 walked segment by segment -- own band from the fresh state,
 //                 the keys before and after it from the stale state -- so each
 //                 tile has one source; a segment's ragged last tile is aligned
@@ -50,12 +53,11 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 608;  // 19 warps: producer, two MMA issuers, 16 softmax
-constexpr int KS = 4, VS = 4;  // K and V ring depths
+constexpr int KVS = 5;  // K/V ring depth (a stage holds a key tile's K and V)
 constexpr uint32_t TILE_BYTES = 128 * 128;  // 128 rows x 64 fp16
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
-constexpr uint32_t OFF_V = OFF_K + KS * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_V + VS * TILE_BYTES;
+constexpr uint32_t OFF_KV = OFF_Q + 2 * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_KV + KVS * 2 * TILE_BYTES;
 constexpr uint32_t OFF_TAB = OFF_BAR + 512;
 constexpr int kTabTiles = 1024;  // key tiles described in shared memory (more: computed)
 constexpr uint32_t SMEM_BYTES = OFF_TAB + kTabTiles * 16 + 1024;
@@ -216,9 +218,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *q_full = bars;
-  uint64_t *k_full = bars + 1, *k_empty = k_full + KS;
-  uint64_t *v_full = k_empty + KS, *v_empty = v_full + VS;
-  uint64_t *s_full = v_empty + VS, *s_empty = s_full + 2;
+  uint64_t *kv_full = bars + 1, *kv_empty = kv_full + KVS;
+  uint64_t *s_full = kv_empty + KVS, *s_empty = s_full + 2;
   uint64_t *p_full = s_empty + 2, *p_empty = p_full + 2;
   uint64_t *o_final = p_empty + 2, *drain = o_final + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 2);
@@ -243,8 +244,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     // a K or V slot is free once every query tile's MMAs have read it
-    for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], ntile); }
-    for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], ntile); }
+    // (S and PV MMAs of every query tile)
+    for (int i = 0; i < KVS; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 2 * ntile); }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&s_empty[t], 8);  // one arrival per softmax warp of the tile
@@ -273,7 +274,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   if (warp == 0) {  // ------------------------------------------------ producer
     // The whole warp runs the loop (warp-uniform operands); one elected lane
     // issues each copy.
-    uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
+    uint32_t kv_armed = 0, kv_par = 0;
     mbar_arrive_expect_tx_w(q_full, ntile * TILE_BYTES);
     tma_load_2d_w(smem + OFF_Q, &tmQ, q_full, head * 64, b * p.Nq + q0);
     if (ntile == 2)
@@ -282,25 +283,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const KvTile kt = kv_tile(j);
       const CUtensorMap *m = kt.fresh ? &tmF : &tmS;
       const int row = b * p.Nkv + kt.kv0;
-      const int ks = j % KS, vs = j % VS;
-      const uint32_t kph = (j / KS) & 1, vph = (j / VS) & 1;
-      if (!mbar_wait_w(&k_empty[ks], kph ^ 1u, abort_flag, p.status)) break;
-      mbar_arrive_expect_tx_w(&k_full[ks], TILE_BYTES);
-      k_armed |= 1u << ks;
-      k_par = (k_par & ~(1u << ks)) | (kph << ks);
-      tma_load_2d_w(smem + OFF_K + ks * TILE_BYTES, m, &k_full[ks], head * 64, row);
-      if (!mbar_wait_w(&v_empty[vs], vph ^ 1u, abort_flag, p.status)) break;
-      mbar_arrive_expect_tx_w(&v_full[vs], TILE_BYTES);
-      v_armed |= 1u << vs;
-      v_par = (v_par & ~(1u << vs)) | (vph << vs);
-      tma_load_2d_w(smem + OFF_V + vs * TILE_BYTES, m, &v_full[vs], p.C + head * 64, row);
+      const int ks = j % KVS;
+      const uint32_t kph = (j / KVS) & 1;
+      if (!mbar_wait_w(&kv_empty[ks], kph ^ 1u, abort_flag, p.status)) break;
+      mbar_arrive_expect_tx_w(&kv_full[ks], 2 * TILE_BYTES);
+      kv_armed |= 1u << ks;
+      kv_par = (kv_par & ~(1u << ks)) | (kph << ks);
+      // one box: the tile's K rows, then its V rows
+      tma_load_3d_w(smem + OFF_KV + ks * 2 * TILE_BYTES, m, &kv_full[ks], head * 64, row, 0);
     }
     if (*abort_flag) {  // copies in flight must land before the CTA exits
       mbar_drain(q_full, 0);
-      for (int i = 0; i < KS; ++i)
-        if ((k_armed >> i) & 1u) mbar_drain(&k_full[i], (k_par >> i) & 1u);
-      for (int i = 0; i < VS; ++i)
-        if ((v_armed >> i) & 1u) mbar_drain(&v_full[i], (v_par >> i) & 1u);
+      for (int i = 0; i < KVS; ++i)
+        if ((kv_armed >> i) & 1u) mbar_drain(&kv_full[i], (kv_par >> i) & 1u);
     }
   } else if ((warp == 1 || warp == 2) && warp - 1 < ntile) {  // --- MMA issuer of tile t
     // Each query tile has its own issuing warp, so one tile's wait for its
@@ -311,26 +306,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int t = warp - 1;
     constexpr uint32_t IDESC_S = idesc_f16(128, 128, false);
     constexpr uint32_t IDESC_O = idesc_f16(128, 64, false, true);
-    const uint32_t sQ = smem_u32(smem + OFF_Q) + t * TILE_BYTES, sK = smem_u32(smem + OFF_K);
-    const uint32_t sV = smem_u32(smem + OFF_V);
+    const uint32_t sQ = smem_u32(smem + OFF_Q) + t * TILE_BYTES;
+    const uint32_t sK = smem_u32(smem + OFF_KV), sV = sK + TILE_BYTES;
     const uint32_t dS = tmem + t * 256, dO = dS + 128, aP = dS + 192;
     auto pv = [&](int j) -> bool {  // O += P(j) V(j)
-      if (!mbar_wait_w(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status)) return false;
+      // (the stage's K/V landed before S(j) was issued and stays until this
+      // PV has read it)
       if (!mbar_wait_w(&p_full[t], j & 1, abort_flag, p.status)) return false;
       tc_fence_after();
-      issue_pv(dO, aP, desc_sw128_mnmajor(sV + (j % VS) * TILE_BYTES, 1024), IDESC_O,
-               j == 0 ? 1u : 0u, &p_empty[t], &v_empty[j % VS]);
+      issue_pv(dO, aP, desc_sw128_mnmajor(sV + (j % KVS) * 2 * TILE_BYTES, 1024), IDESC_O,
+               j == 0 ? 1u : 0u, &p_empty[t], &kv_empty[j % KVS]);
       return true;
     };
     bool ok = mbar_wait_w(q_full, 0, abort_flag, p.status);
     const uint64_t ad = desc_sw128_kmajor(sQ);
     for (int j = 0; ok && j < T; ++j) {
-      ok = mbar_wait_w(&k_full[j % KS], (j / KS) & 1, abort_flag, p.status) &&
+      ok = mbar_wait_w(&kv_full[j % KVS], (j / KVS) & 1, abort_flag, p.status) &&
            mbar_wait_w(&s_empty[t], (j & 1) ^ 1u, abort_flag, p.status);
       if (!ok) break;
       tc_fence_after();
-      issue_s(dS, ad, desc_sw128_kmajor(sK + (j % KS) * TILE_BYTES), IDESC_S, &s_full[t],
-              &k_empty[j % KS]);
+      issue_s(dS, ad, desc_sw128_kmajor(sK + (j % KVS) * 2 * TILE_BYTES), IDESC_S, &s_full[t],
+              &kv_empty[j % KVS]);
       if (j > 0) ok = pv(j - 1);
     }
     if (ok && T > 0) ok = pv(T - 1);
@@ -477,13 +473,16 @@ cudaError_t launch_attn_tc(const AttnArgs &a, int *status, cudaStream_t s) {
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  const uint64_t dims[2] = {(uint64_t)a.C * 2, (uint64_t)a.B * a.Nkv};
-  const uint64_t str[1] = {(uint64_t)a.C * 4};
-  const uint32_t box[2] = {64, 128};
-  if (!encode_tiled(&mf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.kv_fresh, dims, str, box,
+  // K/V state [B * Nkv][K | V] viewed as {channel, token, K or V}: one box
+  // of 64 channels x 128 tokens x both planes lands as the K tile followed
+  // by the V tile
+  const uint64_t dims[3] = {(uint64_t)a.C, (uint64_t)a.B * a.Nkv, 2};
+  const uint64_t str[2] = {(uint64_t)a.C * 4, (uint64_t)a.C * 2};
+  const uint32_t box[3] = {64, 128, 2};
+  if (!encode_tiled(&mf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.kv_fresh, dims, str, box,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (!encode_tiled(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+  if (!encode_tiled(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                     a.kv_stale ? a.kv_stale : a.kv_fresh, dims, str, box,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
