@@ -9,11 +9,15 @@ profiling needs (ncu -k ... -s <warm-up launches> -c ...).
     python -m displaced_patch_parallelism_02_b300.opbench attn --B 2 --H 240 --W 240 --P 8
     python -m displaced_patch_parallelism_02_b300.opbench groupnorm --B 2 --H 480 --W 480 \
         --C 320 --P 8 --flush
+    python -m displaced_patch_parallelism_02_b300.opbench cross --B 2 --H 240 --W 240 \
+        --heads 10 --n_ctx 77 --c_ctx 2048
 
 `attn` is one displaced self-attention call (QKV projection, core, output
 projection); its figure is the attention core alone, timed by the events the
 library records around the core launch (dpp_set_attn_core_events), FLOPs
-4 * B * N^2 * 64 * heads.
+4 * B * N^2 * 64 * heads.  `cross` is one cross-attention call against a
+prompt's context K/V projected once beforehand (dpp_cross_attn_cached); its
+figure is again the core alone, FLOPs 4 * B * N * n_ctx * 64 * heads.
 
 Inputs are seeded random device tensors (bf16 activations, weights scaled by
 1/sqrt(fan_in), fp32 guidance maps); `--warmup` calls run first, then `--reps`
@@ -30,9 +34,10 @@ import json
 import torch
 
 from . import (DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_attn_desc, dpp_cfg_combine,
-               dpp_cfg_workspace_bytes, dpp_conv3x3_gn, dpp_conv_desc, dpp_device_status,
-               dpp_gn_desc, dpp_groupnorm, dpp_groupnorm_apply, dpp_groupnorm_workspace_bytes,
-               dpp_layernorm, dpp_linear, dpp_linear_desc,
+               dpp_cfg_workspace_bytes, dpp_conv3x3_gn, dpp_conv_desc,
+               dpp_cross_attn_cached, dpp_cross_attn_cached_workspace_bytes, dpp_cross_attn_kv,
+               dpp_device_status, dpp_gn_desc, dpp_groupnorm, dpp_groupnorm_apply,
+               dpp_groupnorm_workspace_bytes, dpp_layernorm, dpp_linear, dpp_linear_desc,
                dpp_ln_desc, dpp_self_attn, dpp_self_attn_workspace_bytes,
                dpp_set_attn_core_events)
 
@@ -107,6 +112,29 @@ def setup(args, gen):
             dpp_set_attn_core_events(None, None)
         call.core_events = ev
         return call, 4.0 * B * N * N * 64 * heads, "TFLOP/s"
+    if args.op == "cross":  # cross-attention against a prompt's context K/V
+        B, H, W, heads, L, Cc = args.B, args.H, args.W, args.heads, args.n_ctx, args.c_ctx
+        C, N = 64 * heads, args.H * args.W
+        x = _randn((B, N, C), gen)
+        ctx = _randn((B, L, Cc), gen)
+        wq, wo = (_randn((C, C), gen, C ** -0.5) for _ in range(2))
+        wk, wv = (_randn((C, Cc), gen, Cc ** -0.5) for _ in range(2))
+        d = dpp_attn_desc(B, H, W, C, heads, 64, 1, L, Cc, DPP_BF16, 0, 0)
+        kv = torch.empty((B, L, 2, C), dtype=torch.float16, device="cuda")
+        dpp_cross_attn_kv(d, ctx, wk, wv, kv)  # once per prompt
+        nws = dpp_cross_attn_cached_workspace_bytes(d)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        y = torch.empty_like(x)
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for e in ev:  # creates the CUDA events; the library re-records them
+            e.record()
+
+        def call():
+            dpp_set_attn_core_events(*ev)
+            dpp_cross_attn_cached(d, x, kv, wq, wo, y, ws, nws)
+            dpp_set_attn_core_events(None, None)
+        call.core_events = ev
+        return call, 4.0 * B * N * L * 64 * heads, "TFLOP/s"
     if args.op == "groupnorm":  # the displaced step, sums of its own input
         B, H, W, C, P, G = args.B, args.H, args.W, args.C, args.P, args.G
         x = _randn((B, H, W, C), gen)
@@ -124,7 +152,8 @@ def setup(args, gen):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm", "attn", "groupnorm"])
+    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm", "attn", "groupnorm",
+                                   "cross"])
     ap.add_argument("--M", type=int, default=115200)
     ap.add_argument("--K", type=int, default=640)
     ap.add_argument("--N", type=int, default=640)
@@ -140,6 +169,8 @@ def main(argv=None):
     ap.add_argument("--G", type=int, default=32)
     ap.add_argument("--T", type=int, default=262144)
     ap.add_argument("--heads", type=int, default=10)
+    ap.add_argument("--n_ctx", type=int, default=77)
+    ap.add_argument("--c_ctx", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--reps", type=int, default=1)
     ap.add_argument("--flush", action="store_true",
