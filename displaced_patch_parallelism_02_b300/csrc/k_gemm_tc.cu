@@ -290,20 +290,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int v = 0; v < 4; ++v)
             res[v] = in && p.accumulate ? reinterpret_cast<const uint4 *>(dst)[v]
                                         : make_uint4(0u, 0u, 0u, 0u);
-          float4 bv[8], bg[8];
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            bv[v] = p.bias ? __ldg(reinterpret_cast<const float4 *>(p.bias + n) + v)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-            bg[v] = p.bias ? __ldg(reinterpret_cast<const float4 *>(p.bias + p.N + n) + v)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
           tmem_wait_ld();
-          const float *bvf = reinterpret_cast<const float *>(bv);
-          const float *bgf = reinterpret_cast<const float *>(bg);
           if (in) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
+              // this 8-column group's value and gate biases (broadcast loads)
+              float4 b4[4] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f),
+                              make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+              if (p.bias) {
+                const float4 *bv = reinterpret_cast<const float4 *>(p.bias + n + 8 * v);
+                const float4 *bg = reinterpret_cast<const float4 *>(p.bias + p.N + n + 8 * v);
+                b4[0] = __ldg(bv);
+                b4[1] = __ldg(bv + 1);
+                b4[2] = __ldg(bg);
+                b4[3] = __ldg(bg + 1);
+              }
+              const float *bvf = reinterpret_cast<const float *>(&b4[0]);
+              const float *bgf = reinterpret_cast<const float *>(&b4[2]);
               const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
               uint4 o;
               uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
@@ -313,8 +316,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int k = v * 8 + 2 * e + h;
-                  const float a = __uint_as_float(rv[k]) + bvf[k];
-                  const float g = __uint_as_float(rg[k]) + bgf[k];
+                  const float a = __uint_as_float(rv[k]) + bvf[2 * e + h];
+                  const float g = __uint_as_float(rg[k]) + bgf[2 * e + h];
                   f[h] = a * (0.5f * g * (1.f + erff(g * 0.70710678118654752f)));
                 }
                 f[0] += __uint_as_float(rw[e] << 16);
