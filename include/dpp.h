@@ -25,11 +25,13 @@
  * Conventions for every entry point:
  *   - Memory: all tensor pointers are DEVICE pointers owned by the caller,
  *     16-byte aligned, dense (no strides).  The library never allocates
- *     device memory and keeps no state between calls except a host-side
- *     cache of TMA tensor maps keyed by (pointer, shape), a launch counter
- *     and the optional profiling events of dpp_set_attn_core_events().  Workspace, where
- *     needed, is passed in by the caller; its size comes from the matching
- *     *_workspace_bytes() query.
+ *     device memory and keeps no state between calls except the per-device
+ *     entries listed under Devices below, a launch counter and the
+ *     optional profiling events of dpp_set_attn_core_events().  TMA tensor
+ *     maps are encoded on the host at every call, so nothing is keyed by a
+ *     pointer that the caller may free.  Workspace, where needed, is passed
+ *     in by the caller; its size comes from the matching *_workspace_bytes()
+ *     query.
  *   - Layout: activations NHWC [B, H, W, C] (torch channels_last); attention
  *     tokens [B, N, C] with N = H*W and token n = h*W + w, so band p owns
  *     the contiguous tokens [p*N/P, (p+1)*N/P).  Channel c of an attention
@@ -50,8 +52,8 @@
  *     dpp_device_status(); an attention layer of type DPP_BF16 whose Q, K
  *     or V leaves the fp16 range records DPP_ERR_RANGE there.
  *   - Devices: the library keeps, per device, the address of its device
- *     status word and of the static GroupNorm scratch, and the shared-memory
- *     limits it has set on its kernels.  These belong to the device's
+ *     status word and of the static GroupNorm scratch, the shared-memory
+ *     limits it has set on its kernels and the GroupNorm launch's occupancy.  These belong to the device's
  *     primary context: do not use the library across cudaDeviceReset
  *     (reload the library in a new process instead).
  *   - Synchronous step: passing NULL as the stale input (stale_prev,
