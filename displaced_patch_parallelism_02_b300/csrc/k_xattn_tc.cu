@@ -19,17 +19,18 @@
 //               rounded to 16, K 64) into one of two TMEM buffers, and once
 //               the softmax has written P_i, O_i = P_i V (M 128, N 64, K keys;
 //               P from TMEM, V MN-major from shared memory);
-//   warps 2..9  two groups of four warps, one per TMEM buffer, taking
-//               alternate tiles; one thread per query row: S row from TMEM
-//               (read twice: once for the row max, once for P), keys past the
-//               end masked, p = 2^(s * scale - max) as fp16 pairs on the
-//               special-function unit, row sum, P back to TMEM; then the
-//               tile's O / l as fp16 through shared memory and one bulk
-//               tensor store per warp.  While one group waits on its
-//               tile's MMAs or memory the other converts, and the MMAs of
-//               one tile run under the other tile's softmax.
-// TMEM per buffer a (256 columns at a * 256): S [0, 128), P [128, 192)
-// (fp16 pairs), O [192, 256).
+//   warps 2..   NB groups of four warps (NB = 3 when the keys round up to at
+//               most 96, else 2), one per TMEM buffer, taking the tiles in
+//               turn; one thread per query row: S row from TMEM (read twice:
+//               once for the row max, then 32 keys at a time for P), keys
+//               past the end masked, p = 2^(s * scale - max) as fp16 pairs on
+//               the special-function unit, row sum, P written over the S
+//               columns already read; then the tile's O / l as fp16 through
+//               shared memory and one bulk tensor store per warp.  The
+//               issuer runs S up to NB - 1 tiles ahead of PV, so every group
+//               has a tile while the others wait on MMAs or memory.
+// TMEM per buffer a (at a * kBuf): S, then P over it, in [0, kSP); O in
+// [kSP, kSP + 64).
 #include "tc_common.cuh"
 
 namespace dpp {
@@ -37,16 +38,26 @@ namespace {
 
 using namespace tc;
 
-constexpr int kXThreads = 320;  // producer, MMA issuer, two groups of four softmax warps
 constexpr int QS = 4;           // Q ring depth
 constexpr uint32_t QTILE = 128 * 128;   // 128 queries x 64 fp16
 constexpr uint32_t KVSLOT = 2 * 128 * 128;  // K and V of up to 128 keys
+constexpr uint32_t kStageBytes = 32 * 128;  // one warp's 32 output rows x 64 fp16
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_KV = OFF_Q + QS * QTILE;
-constexpr uint32_t kStageBytes = 32 * 128;  // one warp's 32 output rows x 64 fp16
-constexpr uint32_t OFF_STAGE = OFF_KV + 2 * KVSLOT;  // 8 warps x 2 buffers
-constexpr uint32_t OFF_BAR = OFF_STAGE + 8 * 2 * kStageBytes;
-constexpr uint32_t XSMEM_BYTES = OFF_BAR + 256 + 1024;
+constexpr uint32_t OFF_STAGE = OFF_KV + 2 * KVSLOT;  // one staging buffer per softmax warp
+
+// NB TMEM buffers, each served by its own group of four softmax warps.  A
+// buffer holds S (keys rounded up to 16) with P written over it, then O:
+// 96 + 64 columns when the keys round to at most 96 (three buffers fit the
+// 512 columns), 128 + 64 otherwise (two).
+template <int NB>
+struct XCfg {
+  static constexpr int kThreads = 64 + 128 * NB;
+  static constexpr uint32_t kSP = NB == 3 ? 96 : 128;  // S / P columns
+  static constexpr uint32_t kBuf = kSP + 64;           // + O
+  static constexpr uint32_t kOffBar = OFF_STAGE + 4 * NB * kStageBytes;
+  static constexpr uint32_t kSmem = kOffBar + 256 + 1024;
+};
 
 struct XattnParams {
   int B, Nq, Nkv, C, heads;
@@ -146,18 +157,32 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
       : "memory");
 }
 
-__global__ void __launch_bounds__(kXThreads, 1)
+// 32 lanes x 16 consecutive 32-bit columns to TMEM: lane i writes TMEM lane
+// (base lane + i), columns [col, col + 16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+template <int NB>
+__global__ void __launch_bounds__(XCfg<NB>::kThreads, 1)
 xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                 const __grid_constant__ CUtensorMap tmO, const XattnParams p) {
+  using Cfg = XCfg<NB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
   uint64_t *q_full = bars, *q_empty = q_full + QS;
   uint64_t *kv_full = q_empty + QS, *kv_empty = kv_full + 2;
-  uint64_t *s_full = kv_empty + 2, *s_free = s_full + 2;
-  uint64_t *p_full = s_free + 2, *o_full = p_full + 2, *o_free = o_full + 2;
-  uint64_t *drain = o_free + 2;
+  uint64_t *s_full = kv_empty + 2, *p_full = s_full + NB;
+  uint64_t *o_full = p_full + NB, *o_free = o_full + NB;
+  uint64_t *drain = o_free + NB;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -174,9 +199,10 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);  // one arrival per softmax warp
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], 4);  // one arrival per softmax warp of the group
       mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], 4);
     }
@@ -236,27 +262,26 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if ((armed >> (4 + i)) & 1u) mbar_drain(&kv_full[i], (par >> (4 + i)) & 1u);
     }
   } else if (warp == 1) {  // ---------------------------------------- MMA issuer
+    constexpr int L = NB - 1;  // S runs this many tiles ahead of PV
     const uint32_t idesc_s = idesc_f16(128, p.nkv16, false);
     constexpr uint32_t IDESC_O = idesc_f16(128, 64, false, true);
     const int ksteps = p.nkv16 / 16;
     int qs = 0;
     uint32_t qph = 0;
     int pairs = 0, cur = -1, slot = 0;
-    int prev_slot = 0, prev_last = 0;  // the previous item's K/V slot, last of its run
+    uint32_t hist = 0;  // 2 bits per recent item: its K/V slot, last of its run
     bool ok = true;
-    // O_j = P_j V of item j (buffer j & 1); frees the K/V slot after the
-    // last item of a (batch, head)
-    auto pv = [&](int j, int kslot, int last) -> bool {
-      const int a = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait_w(&p_full[a], ph, abort_flag, p.status)) return false;
-      if (!mbar_wait_w(&o_free[a], ph ^ 1u, abort_flag, p.status)) return false;
+    // O_j = P_j V of item j (P over S in buffer j % NB); frees the K/V slot
+    // after the last item of a (batch, head)
+    auto pv = [&](int j, uint32_t info) -> bool {
+      const int a = j % NB;
+      if (!mbar_wait_w(&p_full[a], (j / NB) & 1, abort_flag, p.status)) return false;
       tc_fence_after();
-      const uint32_t dO = tmem + a * 256 + 192, aP = tmem + a * 256 + 128;
+      const int kslot = info & 1;
       const uint32_t sV = smem_u32(smem + OFF_KV + kslot * KVSLOT) + kv_plane;
-      const uint64_t vd = desc_sw128_mnmajor(sV, 1024);
-      issue_pv_n(dO, aP, vd, IDESC_O, ksteps, &o_full[a]);
-      if (last) mma_commit_w(&kv_empty[kslot]);
+      const uint32_t tb = tmem + a * Cfg::kBuf;
+      issue_pv_n(tb + Cfg::kSP, tb, desc_sw128_mnmajor(sV, 1024), IDESC_O, ksteps, &o_full[a]);
+      if (info & 2u) mma_commit_w(&kv_empty[kslot]);
       return true;
     };
     int li = 0;
@@ -268,44 +293,43 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         cur = pair;
         ++pairs;
       }
-      const int a = li & 1;
+      const int a = li % NB;
       if (!mbar_wait_w(&q_full[qs], qph, abort_flag, p.status)) break;
-      if (!mbar_wait_w(&s_free[a], ((li >> 1) & 1) ^ 1u, abort_flag, p.status)) break;
+      // the buffer's previous tile (li - NB) is out: its O read, and so its
+      // PV, which read the P written over S, complete
+      if (!mbar_wait_w(&o_free[a], ((li / NB) & 1) ^ 1u, abort_flag, p.status)) break;
       tc_fence_after();
       const uint64_t ad = desc_sw128_kmajor(smem_u32(smem + OFF_Q + qs * QTILE));
       const uint64_t bd = desc_sw128_kmajor(smem_u32(smem + OFF_KV + slot * KVSLOT));
-      issue_s4(tmem + a * 256, ad, bd, idesc_s, &s_full[a], &q_empty[qs]);
+      issue_s4(tmem + a * Cfg::kBuf, ad, bd, idesc_s, &s_full[a], &q_empty[qs]);
       if (++qs == QS) {
         qs = 0;
         qph ^= 1u;
       }
-      if (li > 0) ok = pv(li - 1, prev_slot, prev_last);
-      prev_slot = slot;
-      prev_last = item + 1 == end || (item + 1) / p.tpq != pair;
+      const uint32_t last = item + 1 == end || (item + 1) / p.tpq != pair;
+      hist = (hist << 2) | (uint32_t)slot | (last << 1);
+      if (li >= L) ok = pv(li - L, (hist >> (2 * L)) & 3u);
     }
-    if (ok && li > 0 && !*abort_flag) ok = pv(li - 1, prev_slot, prev_last);
+    // the last L tiles' PV
+    for (int t = L; ok && t >= 1 && !*abort_flag; --t)
+      if (li - t >= 0) ok = pv(li - t, (hist >> (2 * (t - 1))) & 3u);
     if (*abort_flag || !ok) {  // nothing may still be writing TMEM when it is freed
       mma_commit_w(drain);
       mbar_drain(drain, 0);
     }
   } else {  // ------------------------------------------------ softmax, epilogue
-    // Two groups of four warps, one per TMEM buffer: group g takes the items
-    // with local index = g (mod 2), so one group's softmax and epilogue
-    // latency overlaps the other's.  One thread per query row.
-    const int g = (warp - 2) >> 2;
-    const int quad = warp & 3;  // TMEM lanes this warp may access
-    const int r = quad * 32 + lane;
-    const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + g * 256;
-    const uint32_t tS = tq, tP = tq + 128, tO = tq + 192;
+    const int g = (warp - 2) >> 2;  // group = TMEM buffer
+    const int quad = warp & 3;      // TMEM lanes this warp may access
+    const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + g * Cfg::kBuf;
+    const uint32_t tS = tq, tO = tq + Cfg::kSP;  // P is written over S
     const int nch = (p.nkv16 + 31) / 32;  // 32-column chunks of S
-    // this warp's two output staging buffers (32 rows x 128 bytes each)
-    uint8_t *stage = smem + OFF_STAGE + (warp - 2) * 2 * kStageBytes;
+    uint8_t *stage = smem + OFF_STAGE + (warp - 2) * kStageBytes;  // this warp's
     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
     int k = 0;
-    for (int item = begin + g; item < end; item += 2, ++k) {
+    for (int item = begin + g; item < end; item += NB, ++k) {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[g], k & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      // pass 1: the row max over the keys (columns past them count as -inf)
+      // pass 1: the row max over the keys (columns past them do not count)
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {  // 64 columns per load group, one wait each
@@ -336,31 +360,27 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       const float m2 = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
       const float2 nm2 = make_float2(-m2, -m2);
-      // pass 2: P = 2^(s * scale - max) as fp16 pairs (ex2 of an fp16 pair on
-      // the special-function unit), 64 keys -> 32 P columns at a time; the
-      // row sum in paired fp16 adds (four chains), folded into fp32
+      // pass 2, 32 keys at a time: P = 2^(s * scale - max) as fp16 pairs (ex2
+      // of an fp16 pair on the special-function unit) into 16 columns over
+      // the S columns already read (chunk c writes [16c, 16c + 16), below
+      // the next chunk's [32(c+1), ...)); the row sum in paired fp16 adds,
+      // four chains per chunk, folded into fp32
       float l = 0.f;
 #pragma unroll
-      for (int pc = 0; pc < 2; ++pc) {
-        if (2 * pc >= nch) continue;
-        uint32_t sr[64];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (2 * pc + h < nch) tmem_ld32(tS + 64 * pc + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * h]));
-          else
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sr[32 * h + i] = 0xff800000u;
-        }
+      for (int c = 0; c < 4; ++c) {
+        if (c >= nch) continue;
+        uint32_t ch[32];
+        tmem_ld32(tS + 32 * c, ch);
         tmem_wait_ld();
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = 64 * pc + 2 * i;
+        for (int i = 0; i < 16; ++i) {
+          const int key = 32 * c + 2 * i;
           if (key >= p.nkv16) {  // past the MMA's K: no exponential needed
             pk[i] = 0u;
             continue;
           }
-          float s0 = __uint_as_float(sr[2 * i]), s1 = __uint_as_float(sr[2 * i + 1]);
+          float s0 = __uint_as_float(ch[2 * i]), s1 = __uint_as_float(ch[2 * i + 1]);
           if (key + 2 > p.Nkv) {  // uniform: only the pairs at the end of the keys
             s0 = key < p.Nkv ? s0 : -INFINITY;
             s1 = key + 1 < p.Nkv ? s1 : -INFINITY;
@@ -372,20 +392,17 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[j] = *reinterpret_cast<const __half2 *>(&pk[j]);
 #pragma unroll
-        for (int i = 4; i < 32; ++i)
+        for (int i = 4; i < 16; ++i)
           acc[i & 3] = __hadd2(acc[i & 3], *reinterpret_cast<const __half2 *>(&pk[i]));
         const float2 a0 = __half22float2(acc[0]), a1 = __half22float2(acc[1]);
         const float2 a2 = __half22float2(acc[2]), a3 = __half22float2(acc[3]);
         l += ((a0.x + a0.y) + (a1.x + a1.y)) + ((a2.x + a2.y) + (a3.x + a3.y));
-        // P of item k may overwrite item k-1's: its PV finished before that
-        // item's epilogue (below) read O
-        tmem_st32(tP + 32 * pc, pk);
+        tmem_st16(tS + 16 * c, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      arrive_w(&s_free[g]);  // S fully read
       arrive_w(&p_full[g]);
-      // epilogue: O / l to global memory (fp16), then the O columns are free
+      // epilogue: O / l to global memory (fp16), then the buffer is free
       if (!__all_sync(0xffffffffu, mbar_wait(&o_full[g], k & 1, abort_flag, p.status))) break;
       tc_fence_after();
       uint32_t o[64];
@@ -396,13 +413,12 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       arrive_w(&o_free[g]);
       const int pair = item / p.tpq, qt = item % p.tpq;
       const int b = pair / p.heads, head = pair % p.heads;
-      // The warp's 32 rows x 64 fp16 go through a shared-memory staging
+      // The warp's 32 rows x 64 fp16 go through its shared-memory staging
       // buffer (128-byte rows, 16-byte units swizzled by the row as the
       // tensor map's 128-byte swizzle does: conflict-free) and one bulk
       // tensor store; the {channel, query, batch} map clips rows past Nq.
-      uint8_t *buf = stage + (k & 1) * kStageBytes;
-      if (k >= 2) {  // the store that read this buffer two items ago
-        if (lane == 0) bulk_wait_read<1>();
+      if (k >= 1) {  // this warp's previous store has read the buffer
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
       }
       const float inv = 1.f / l;
@@ -414,12 +430,12 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int e = 0; e < 4; ++e)
           ww[e] = pack_half2(__uint_as_float(o[8 * v + 2 * e]) * inv,
                              __uint_as_float(o[8 * v + 2 * e + 1]) * inv);
-        *reinterpret_cast<uint4 *>(buf + lane * 128 + ((v ^ (lane & 7)) * 16)) = w;
+        *reinterpret_cast<uint4 *>(stage + lane * 128 + ((v ^ (lane & 7)) * 16)) = w;
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && qt * 128 + quad * 32 < p.Nq)  // no store that starts past the end
-        tma_store_3d(&tmO, buf, head * 64, qt * 128 + quad * 32, b);
+        tma_store_3d(&tmO, stage, head * 64, qt * 128 + quad * 32, b);
     }
     if (lane == 0) bulk_wait_all();  // every bulk store has landed before the CTA exits
     __syncwarp();
@@ -475,15 +491,24 @@ cudaError_t launch_xattn_tc(const AttnArgs &a, int *status, cudaStream_t s) {
   const int tpq = (a.Nq + 127) / 128;
   XattnParams p{a.B, a.Nq, a.Nkv, a.C, a.heads, tpq, a.B * a.heads * tpq, nkv16, a.o, status,
                 0.125f * 1.4426950408889634f};
-  cudaError_t e = cudaFuncSetAttribute(xattn_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)XSMEM_BYTES);
-  if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = p.items < sms ? p.items : sms;
-  xattn_tc_kernel<<<grid, kXThreads, XSMEM_BYTES, s>>>(mq, mkv, mo, p);
+  // three TMEM buffers (three softmax groups) when S fits 96 columns
+  if (nkv16 <= 96) {
+    cudaError_t e = cudaFuncSetAttribute(xattn_tc_kernel<3>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)XCfg<3>::kSmem);
+    if (e != cudaSuccess) return e;
+    xattn_tc_kernel<3><<<grid, XCfg<3>::kThreads, XCfg<3>::kSmem, s>>>(mq, mkv, mo, p);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(xattn_tc_kernel<2>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)XCfg<2>::kSmem);
+    if (e != cudaSuccess) return e;
+    xattn_tc_kernel<2><<<grid, XCfg<2>::kThreads, XCfg<2>::kSmem, s>>>(mq, mkv, mo, p);
+  }
   return cudaGetLastError();
 }
 
