@@ -920,20 +920,25 @@ def main():
         if pg:
             pg.barrier()
         # Every step copies its inputs in from pinned host memory and its
-        # results out, all inside the timed region; with two device sets the
-        # copies of one step run on a copy stream while the other set's step
-        # computes (step k+1's inputs are copied once step k-1, the last user
-        # of that set, is done; step k's results once step k is done).
+        # results out, all inside the timed region.  With two device sets the
+        # copies of one step overlap the other set's compute, and the two
+        # directions run on two copy streams (PCIe is full duplex: one stream
+        # would serialise them): step k+1's inputs are copied in once step
+        # k-1, the last reader of that set, is done; step k's results are
+        # copied out once step k is done; step k+2 overwrites step k's result
+        # buffers only after they are copied out.
         step.make_io_sets()
-        cs = torch.cuda.Stream(dev)
+        cs_in, cs_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         in_ready = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        cs.wait_stream(s)
-        e0.record(cs)
+        cs_in.wait_stream(s)
+        cs_out.wait_stream(s)
+        e0.record(cs_in)
         step.select(0)
-        bi = step.h2d(cs)
-        in_ready[0].record(cs)
+        bi = step.h2d(cs_in)
+        in_ready[0].record(cs_in)
         # The sampler's side of each step: once a step's results are on the
         # host, its discrepancy (rel-MAE from the guidance sums) goes to the
         # adaptive switching controller, which names the stage of the steps
@@ -941,10 +946,10 @@ def main():
         # is queued, so the device never idles on it.
         sw = dpp.dpp_switch_state()
         dpp.dpp_switch_init(sw, SWITCH_FLAT_TOL, SWITCH_RISE_TOL, SWITCH_PATIENCE)
-        stages, out_copied = [], torch.cuda.Event()
+        stages = []
 
-        def observe():
-            out_copied.synchronize()
+        def observe(k):
+            out_done[k % 2].synchronize()
             h = step.out_host[3]
             stages.append(dpp.dpp_switch_update(sw, float(h[0] / h[1])))
 
@@ -952,22 +957,25 @@ def main():
             i, j = k % 2, 1 - k % 2
             step.select(i)
             s.wait_event(in_ready[i])
+            if k >= 2:
+                s.wait_event(out_done[i])  # step k-2's results are out of this set
             step.run()
             done[i].record(s)
             if k >= 1:
-                observe()
+                observe(k - 1)
             if k + 1 < K:
                 if k >= 1:
-                    cs.wait_event(done[j])
+                    cs_in.wait_event(done[j])
                 step.select(j)
-                step.h2d(cs)
-                in_ready[j].record(cs)
+                step.h2d(cs_in)
+                in_ready[j].record(cs_in)
                 step.select(i)
-            cs.wait_event(done[i])
-            step.d2h(cs)
-            out_copied.record(cs)
-        observe()
-        e1.record(cs)
+            cs_out.wait_event(done[i])
+            step.d2h(cs_out)
+            out_done[i].record(cs_out)
+        observe(K - 1)
+        cs_out.wait_stream(cs_in)
+        e1.record(cs_out)
         torch.cuda.synchronize(dev)
         step.select(0)
         e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
