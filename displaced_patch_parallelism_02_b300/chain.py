@@ -144,6 +144,39 @@ class BlockChain:
                  + 2.0 * M * C * C)
         return conv + lin + self_attn + cross
 
+    # the displaced states a step publishes for the next one to read
+    STATES = ("g1", "g2", "st1", "st2", "stt", "kv")
+
+    def state_dict(self):
+        """A checkpoint: the step count and the states the next step reads as
+        the previous step's (the conv inputs, the GroupNorm partials and the
+        K/V state the last step published), copied to host memory after the
+        device has finished writing them.  Before the first step there are
+        none: the next step is the synchronous one."""
+        sd = {"k": self.k}
+        if self.k == 0:
+            return sd
+        i = (self.k - 1) % 2  # the buffers the last step wrote
+        torch.cuda.synchronize(self.dev)
+        for name in self.STATES:
+            sd[name] = getattr(self, name)[i].cpu()
+        return sd
+
+    def load_state_dict(self, sd):
+        """Resumes from a checkpoint taken by state_dict on a chain of the same
+        shapes: the next step reads those states as the previous step's, so
+        it computes exactly what the checkpointed chain's next step would."""
+        k = int(sd["k"])
+        if k > 0:
+            i = (k - 1) % 2
+            for name in self.STATES:
+                dst, src = getattr(self, name)[i], sd[name]
+                if tuple(src.shape) != tuple(dst.shape) or src.dtype != dst.dtype:
+                    raise ValueError(f"{name}: checkpoint {tuple(src.shape)} {src.dtype}, "
+                                     f"chain {tuple(dst.shape)} {dst.dtype}")
+                dst.copy_(src)
+        self.k = k
+
     def step(self, x, ctx, stream=None, hook=None):
         """One displaced step on x ([B, H, W, C] bf16, updated in place) with
         the text context ctx ([B, n_ctx, c_ctx] bf16).  hook(op, when, tensors),

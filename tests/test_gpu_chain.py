@@ -307,6 +307,48 @@ def test_chain_launches_only_library_kernels_and_repeats(cuda_device):
     check(outs[1], outs[0], BF16, "repeated input, displaced vs synchronous step")
 
 
+def test_chain_resumes_bit_identical_from_a_checkpoint(cuda_device):
+    """Checkpoint / resume of the displaced states: a chain stepped four times
+    without a break, against one stepped twice, checkpointed to host memory,
+    dropped, and a fresh chain (new device buffers, garbage before the load)
+    resumed from the checkpoint for the last two steps.  The latent and every
+    state the last step publishes are bit-identical."""
+    ch = CH
+    wts = chain_device_weights(wl.chain_weights(ch))
+    xs, ctx = wl.chain_inputs(ch, 3)
+    ctx_d = ctx.to("cuda")
+    args = (ch.B, ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx, wts, "cuda")
+
+    def run(chain, steps, x):
+        for s in steps:
+            x.copy_(x + 0.0 if s == 0 else xs[s].to("cuda") * 0.5 + x * 0.5)
+            chain.step(x, ctx_d)
+        torch.cuda.synchronize()
+        return x
+
+    full = BlockChain(*args, ff_mult=ch.ff_mult)
+    x_full = run(full, range(4), xs[0].to("cuda", copy=True))
+    first = BlockChain(*args, ff_mult=ch.ff_mult)
+    x_part = run(first, range(2), xs[0].to("cuda", copy=True))
+    sd = first.state_dict()
+    assert sd["k"] == 2 and all(name in sd for name in BlockChain.STATES)
+    x_host = x_part.cpu()
+    del first, x_part
+    torch.cuda.empty_cache()
+    resumed = BlockChain(*args, ff_mult=ch.ff_mult)
+    for name in BlockChain.STATES:  # the fresh chain's buffers hold garbage
+        for t in getattr(resumed, name):
+            t.view(torch.uint8).fill_(0x7f)
+    resumed.load_state_dict(sd)
+    x_res = run(resumed, range(2, 4), x_host.to("cuda"))
+    assert dpp.dpp_device_status() == dpp.DPP_OK
+    assert torch.equal(x_res, x_full)
+    got, want = resumed.state_dict(), full.state_dict()
+    assert got["k"] == want["k"] == 4
+    for name in BlockChain.STATES:
+        assert torch.equal(got[name], want[name]), name
+
+
 def test_branch_schedules_agree(cuda_device):
     """Hydiff's condition-based partition on one GPU: the two branches as
     chains of batch 1, serially or on two streams, three steps each (the
