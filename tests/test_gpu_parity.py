@@ -230,6 +230,7 @@ ATTN_CASES = [  # (B, H, W, heads, P, dtype)
     (2, 6, 20, 2, 3, BF16),     # 40 tokens per band: ragged against every tile size
     (1, 16, 16, 4, 4, BF16),
     (1, 12, 12, 2, 3, F32),
+    (1, 8, 10, 5, 2, BF16),     # C 320: each QKV weight block tiled 256 + 64 columns
 ]
 
 
