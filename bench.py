@@ -203,30 +203,33 @@ def l2_flusher(dev):
 def timed(call, stream, reps, warmup=3, flush=None, core=None):
     """Median milliseconds of `reps` calls, each between two CUDA events on
     `stream` (after `warmup` untimed calls); `flush` runs before every timed
-    call, outside its events.  With `core` (a pair of events the library
-    records around the attention core, dpp_set_attn_core_events) the median
-    of the core's own times is returned as well."""
+    call, outside its events.  With `core` (the stream on which to create the
+    events the library records around the attention core,
+    dpp_set_attn_core_events) every rep gets its own pair of core events, so
+    the reps are queued back to back as in a step -- no host synchronisation,
+    and no host launch time, between them -- and the median of the core's own
+    times is returned as well."""
     import displaced_patch_parallelism_02_b300 as dpp
     for _ in range(warmup):
         call()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
-    cores = []
+    cores = [core_event_pair(core) for _ in range(reps)] if core is not None else None
     for i in range(reps):
         if flush:
             flush()
-        if core:
-            dpp.dpp_set_attn_core_events(*core)
+        if cores:
+            dpp.dpp_set_attn_core_events(*cores[i])
         evs[i][0].record(stream)
         call()
         evs[i][1].record(stream)
-        if core:
+        if cores:
             dpp.dpp_set_attn_core_events(None, None)
-            torch.cuda.synchronize()
-            cores.append(core[0].elapsed_time(core[1]))
     torch.cuda.synchronize()
     ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-    return (ms, statistics.median(cores)) if core else ms
+    if cores:
+        return ms, statistics.median(a.elapsed_time(b) for a, b in cores)
+    return ms
 
 
 def core_event_pair(stream):
@@ -363,11 +366,10 @@ class ConfigOps:
         if a:
             core_f = 4.0 * a.B * a.N * a.N * a.head_dim * a.heads
             proj_f = 2.0 * a.B * a.N * a.C * 4 * a.C
-            core = core_event_pair(s)
             ms, cms = timed(lambda: dpp.dpp_self_attn(
                 self.ad, self.xa, self.aw["wq"], self.aw["wk"], self.aw["wv"], self.aw["wo"],
                 self.kv[0], self.kv[1], self.ya, self.aws, self.aws_n, stream=s),
-                s, max(3, reps // 2), core=core)
+                s, max(3, reps // 2), core=s)
             out["self_attn"] = tensor_op(core_f + proj_f, ms, entry="dpp_self_attn")
             out["self_attn_core"] = tensor_op(core_f, cms, entry="attention core alone")
             out["self_attn_projections"] = tensor_op(proj_f, ms - cms,
@@ -376,10 +378,9 @@ class ConfigOps:
                 xf = (2.0 * 2.0 * a.B * a.N * a.C * a.C
                       + 4.0 * a.B * a.N * a.n_ctx * a.head_dim * a.heads)
                 kvf = 2.0 * a.B * a.n_ctx * a.c_ctx * 2 * a.C
-                core = core_event_pair(s)
                 ms, cms = timed(lambda: dpp.dpp_cross_attn_cached(
                     self.xd, self.ya, self.kvc, self.xw["wq"], self.xw["wo"], self.yc,
-                    self.xcws, self.xcws_n, stream=s), s, reps, core=core)
+                    self.xcws, self.xcws_n, stream=s), s, reps, core=s)
                 out["cross_attn"] = tensor_op(xf, ms, entry="dpp_cross_attn_cached (per step)")
                 out["cross_attn_core"] = tensor_op(4.0 * a.B * a.N * a.n_ctx * a.head_dim * a.heads,
                                                    cms, entry="attention core over 77 keys")

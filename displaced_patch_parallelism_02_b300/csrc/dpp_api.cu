@@ -133,17 +133,35 @@ size_t wo16_bytes(const dpp_attn_desc &d) {
   return d.dtype == DPP_BF16 ? align_up((size_t)d.C * d.C * 2, 256) : 0;
 }
 
-// Output projection y = O wo^T; for bf16 layers wo is first cast to fp16
-// into `wo16` so both operands are fp16.
+// The first projection of a bf16 attention layer (QKV, or cross-attention's
+// Q) also makes the fp16 copy of wo the output projection needs, as a side
+// task of the GEMM's epilogue warps: one launch fewer per call.  Returns
+// whether the copy was attached (the tensor-core GEMM runs this shape).
+bool attach_wo16(GemmArgs &g, const dpp_attn_desc &d, const void *wo, void *wo16) {
+  if (d.dtype != DPP_BF16) return false;
+  g.cast_src = wo;
+  g.cast_dst = wo16;
+  g.cast_n = (size_t)d.C * d.C;
+  if (gemm_tc_supported(g)) return true;
+  g.cast_src = nullptr;
+  g.cast_dst = nullptr;
+  g.cast_n = 0;
+  return false;
+}
+
+// Output projection y = O wo^T; for bf16 layers wo is cast to fp16 into
+// `wo16` (unless the first projection already did) so both operands are fp16.
 cudaError_t out_proj(const dpp_attn_desc &d, const void *o, const void *wo, void *wo16, void *y,
-                     int M, cudaStream_t s) {
+                     int M, cudaStream_t s, bool wo16_ready) {
   const Elem te = inter_elem(d.dtype), tl = layer_elem(d.dtype);
   const int C = d.C;
   const void *w = wo;
   Elem tw = tl;
   if (d.dtype == DPP_BF16) {
-    cudaError_t e = counted(launch_cast_bf16_f16(wo, wo16, (size_t)C * C, s), 1);
-    if (e != cudaSuccess) return e;
+    if (!wo16_ready) {
+      cudaError_t e = counted(launch_cast_bf16_f16(wo, wo16, (size_t)C * C, s), 1);
+      if (e != cudaSuccess) return e;
+    }
     w = wo16;
     tw = E_F16;
   }
@@ -394,6 +412,8 @@ dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, 
   const int M = (int)nt;
   // 1. Q for every token (every band's own queries), fresh K/V into kv_next
   GemmArgs qkv{x, {wq, wk, wv}, C, M, 3 * C, C, q, C, C, kv_next, 2 * C, tl, tl, te};
+  void *wo16 = wsb + 2 * align_up(nq, 256);
+  const bool wo16_ready = attach_wo16(qkv, *d, wo, wo16);
   cudaError_t e = gemm(qkv, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 2. displaced attention core
@@ -402,7 +422,7 @@ dpp_status dpp_self_attn(const dpp_attn_desc *d, const void *x, const void *wq, 
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   // 3. output projection
-  return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256), y, M, s));
+  return from_cuda(out_proj(*d, o, wo, wo16, y, M, s, wo16_ready));
 }
 
 dpp_status dpp_cross_attn_kv(const dpp_attn_desc *d, const void *ctx, const void *wk,
@@ -459,12 +479,14 @@ dpp_status dpp_cross_attn_cached(const dpp_attn_desc *d, const void *x, const vo
   void *o = wsb + align_up(nq, 256);
   const int C = d->C;
   GemmArgs qg{x, {wq, nullptr, nullptr}, C, (int)nt, C, C, q, C, C, nullptr, 0, tl, tl, te};
+  void *wo16 = wsb + 2 * align_up(nq, 256);
+  const bool wo16_ready = attach_wo16(qg, *d, wo, wo16);
   cudaError_t e = gemm(qg, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
   AttnArgs a{q, kv_ctx, nullptr, o, d->B, d->H * d->W, d->n_ctx, C, d->heads, 1, te, 0};
   e = attn_core(a, s);
   if (e != cudaSuccess) return DPP_ERR_CUDA;
-  return from_cuda(out_proj(*d, o, wo, wsb + 2 * align_up(nq, 256), y, (int)nt, s));
+  return from_cuda(out_proj(*d, o, wo, wo16, y, (int)nt, s, wo16_ready));
 }
 
 dpp_status dpp_cross_attn(const dpp_attn_desc *d, const void *x, const void *ctx, const void *wq,

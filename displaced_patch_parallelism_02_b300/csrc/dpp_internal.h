@@ -95,6 +95,12 @@ struct GemmArgs {
   int accumulate = 0;           // out0 += result (out0 read first)
   int geglu = 0;                // B[0] = value rows, B[1] = gate rows (b_rows = N each):
                                 // out0 = value * GELU(gate), N output columns
+  // optional side task of the tensor-core GEMM: a bf16 -> fp16 copy of
+  // cast_n elements (a multiple of 8, 16-byte aligned), done by the
+  // epilogue warps while they wait for their first accumulator
+  const void *cast_src = nullptr;
+  void *cast_dst = nullptr;
+  size_t cast_n = 0;
 };
 cudaError_t launch_gemm_simt(const GemmArgs &g, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmArgs &g, int *status, cudaStream_t s);

@@ -80,6 +80,9 @@ struct GemmTcParams {
   int geglu;          // tile = BN/2 value rows of B0 + BN/2 gate rows of B1
   int pf_boxes;       // residual L2 prefetch boxes per tile (0: no residual)
   int pf_cols;        // columns per prefetch box
+  const void *cast_src;  // bf16 -> fp16 side copy (cast_n elements), or null
+  void *cast_dst;
+  size_t cast_n;
 };
 
 constexpr int kEpiWarps = 8;
@@ -257,6 +260,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // 16-byte units swizzled by the row as the 64-byte tensor-map swizzle does)
     uint8_t *stage_o = stage_out + (warp - 2) * 2 * kStageOut;
     int n_stored = 0;  // chunks this warp has handed to the bulk-store engine
+    if (p.cast_n) {
+      // The side copy (the output projection's weight, bf16 -> fp16, for a
+      // later launch) while the first accumulator is still being computed:
+      // 16-byte vectors, grid-strided over every epilogue thread.
+      const size_t nv = p.cast_n / 8;
+      const size_t nthr = (size_t)gridDim.x * kEpiWarps * 32;
+      const uint4 *src = reinterpret_cast<const uint4 *>(p.cast_src);
+      uint4 *dst = reinterpret_cast<uint4 *>(p.cast_dst);
+      for (size_t v = (size_t)blockIdx.x * kEpiWarps * 32 + (threadIdx.x - 64); v < nv;
+           v += nthr) {
+        const uint4 in = __ldg(src + v);
+        const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
+        uint4 o;
+        uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          ow[e] = pack_half2(__uint_as_float(iw[e] << 16), __uint_as_float(iw[e] & 0xffff0000u));
+        dst[v] = o;
+      }
+    }
     int it = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       int n0, w, mat, brow;
@@ -500,7 +523,8 @@ cudaError_t run(const GemmArgs &g, int *status, cudaStream_t s) {
                               : ((g.N + g.b_rows - 1) / g.b_rows) * tpb;
   GemmTcParams p{g.M, g.N, g.K, g.b_rows, g.out0, g.ld0, g.split, g.out1, g.ld1,
                  g.to == E_F16 ? 1 : 0, (g.M + BM - 1) / BM, n_tiles, tpb, status,
-                 g.bias, g.accumulate ? 1 : 0, g.geglu ? 1 : 0, pf_boxes, pf_cols};
+                 g.bias, g.accumulate ? 1 : 0, g.geglu ? 1 : 0, pf_boxes, pf_cols,
+                 g.cast_src, g.cast_dst, g.cast_n};
   // stages, 1024-byte alignment slack, the epilogue warps' staging buffers, barriers
   constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 +
                           (size_t)kEpiWarps * 2 * kStageOut + 256;
@@ -560,6 +584,10 @@ cudaError_t launch_cast_bf16_f16(const void *in, void *out, size_t n, cudaStream
 }
 
 bool gemm_tc_supported(const GemmArgs &g) {
+  if (g.cast_n && (g.cast_n % 8 || !g.cast_src || !g.cast_dst ||
+                   (reinterpret_cast<uintptr_t>(g.cast_src) & 15u) ||
+                   (reinterpret_cast<uintptr_t>(g.cast_dst) & 15u)))
+    return false;
   const bool in16 = (g.ta == E_BF16 || g.ta == E_F16) && g.ta == g.tb;
   const bool out16 = g.to == E_BF16 || g.to == E_F16;
   if (g.bias && (reinterpret_cast<uintptr_t>(g.bias) & 15u)) return false;  // float4 loads
