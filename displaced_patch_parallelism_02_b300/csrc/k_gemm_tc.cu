@@ -85,6 +85,17 @@ struct GemmTcParams {
   size_t cast_n;
 };
 
+// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, 7.1.25:
+// erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3) exp(-x^2) + e(x), t = 1 / (1 + p x),
+// |e(x)| <= 2.5e-5 for x >= 0 (odd extension for x < 0) -- four orders below
+// half a bf16 ulp of the gated-GELU output it feeds.
+__device__ __forceinline__ float erf_as7125(float x) {
+  const float ax = fabsf(x);
+  const float t = __fdividef(1.f, fmaf(0.47047f, ax, 1.f));
+  const float poly = t * fmaf(t, fmaf(t, 0.7478556f, -0.0958798f), 0.3480242f);
+  return copysignf(1.f - poly * __expf(-ax * ax), x);
+}
+
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int BM = 128, BK = 64;
@@ -295,7 +306,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_fence_after();
       if (p.geglu) {
         // value columns [0, BN/2) and gate columns [BN/2, BN) of the
-        // accumulator: out[n0 + j] = (value_j + b_j) * GELU(gate_j + b_{N + j})
+        // accumulator: out[n0 + j] = (value_j + b_j) * GELU(gate_j + b_{N + j}),
+        // staged and stored like the plain epilogue's chunks
         constexpr int CH = BN / 128;  // value chunks per warp
 #pragma unroll 1
         for (int cc = 0; cc < CH; ++cc) {
@@ -306,50 +318,57 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tmem_ld32(ta, rv);
           tmem_ld32(ta + BN / 2, rg);
           const int n = n0 + c * 32;
-          __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out0) + (size_t)m * p.ld0 + n;
-          const bool in = m < p.M;
+          const bool ld = p.accumulate && m < p.M;
           uint4 res[4];  // loads in flight while the accumulator is read
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            res[v] = in && p.accumulate ? reinterpret_cast<const uint4 *>(dst)[v]
-                                        : make_uint4(0u, 0u, 0u, 0u);
+            res[v] = ld ? reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(
+                              p.out0) + (size_t)m * p.ld0 + n)[v]
+                        : make_uint4(0u, 0u, 0u, 0u);
           tmem_wait_ld();
-          if (in) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              // this 8-column group's value and gate biases (broadcast loads)
-              float4 b4[4] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f),
-                              make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-              if (p.bias) {
-                const float4 *bv = reinterpret_cast<const float4 *>(p.bias + n + 8 * v);
-                const float4 *bg = reinterpret_cast<const float4 *>(p.bias + p.N + n + 8 * v);
-                b4[0] = __ldg(bv);
-                b4[1] = __ldg(bv + 1);
-                b4[2] = __ldg(bg);
-                b4[3] = __ldg(bg + 1);
-              }
-              const float *bvf = reinterpret_cast<const float *>(&b4[0]);
-              const float *bgf = reinterpret_cast<const float *>(&b4[2]);
-              const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
-              uint4 o;
-              uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float f[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int k = v * 8 + 2 * e + h;
-                  const float a = __uint_as_float(rv[k]) + bvf[2 * e + h];
-                  const float g = __uint_as_float(rg[k]) + bgf[2 * e + h];
-                  f[h] = a * (0.5f * g * (1.f + erff(g * 0.70710678118654752f)));
-                }
-                f[0] += __uint_as_float(rw[e] << 16);
-                f[1] += __uint_as_float(rw[e] & 0xffff0000u);
-                ow[e] = pack_bf162(f[0], f[1]);
-              }
-              reinterpret_cast<uint4 *>(dst)[v] = o;
-            }
+          uint8_t *buf = stage_o + (n_stored & 1) * kStageOut;
+          if (n_stored >= 2) {  // the store that read this buffer two chunks ago
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
           }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            // this 8-column group's value and gate biases (broadcast loads)
+            float4 b4[4] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f),
+                            make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+            if (p.bias) {
+              const float4 *bv = reinterpret_cast<const float4 *>(p.bias + n + 8 * v);
+              const float4 *bg = reinterpret_cast<const float4 *>(p.bias + p.N + n + 8 * v);
+              b4[0] = __ldg(bv);
+              b4[1] = __ldg(bv + 1);
+              b4[2] = __ldg(bg);
+              b4[3] = __ldg(bg + 1);
+            }
+            const float *bvf = reinterpret_cast<const float *>(&b4[0]);
+            const float *bgf = reinterpret_cast<const float *>(&b4[2]);
+            const uint32_t rw[4] = {res[v].x, res[v].y, res[v].z, res[v].w};
+            uint4 o;
+            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float f[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int k = v * 8 + 2 * e + h;
+                const float a = __uint_as_float(rv[k]) + bvf[2 * e + h];
+                const float g = __uint_as_float(rg[k]) + bgf[2 * e + h];
+                f[h] = a * (0.5f * g * (1.f + erf_as7125(g * 0.70710678118654752f)));
+              }
+              f[0] += __uint_as_float(rw[e] << 16);
+              f[1] += __uint_as_float(rw[e] & 0xffff0000u);
+              ow[e] = pack_bf162(f[0], f[1]);
+            }
+            *reinterpret_cast<uint4 *>(buf + lane * 64 + ((v ^ ((lane >> 1) & 3)) * 16)) = o;
+          }
+          fence_proxy_async_smem();  // the generic-proxy writes, before the bulk copy reads them
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&tmO0, buf, n, m0 + q * 32);  // rows past M clipped
+          ++n_stored;
         }
         tc_fence_before();
         __syncwarp();
