@@ -12,10 +12,11 @@
 // and TMA fills them with zeros: the image padding costs nothing.
 //
 // Persistent, warp-specialised, one CTA per SM (the GEMM kernel's layout):
-//   warp 0      TMA producer (converged warp; an elected lane issues each
-//               copy): A box {64 ch, 128 px} from the fresh or stale
-//               map, B box {64 ch, 1 tap, BN out-ch} of the weights
-//               [C_out][3][3][C_in], 128-byte swizzle, STAGES-deep ring;
+//   warps 0, 6  TMA producers, each owning alternate stages (converged
+//               warps; an elected lane issues each copy): A box {64 ch,
+//               128 px} from the fresh or stale map, B box {64 ch, 1 tap,
+//               BN out-ch} of the weights [C_out][3][3][C_in], 128-byte
+//               swizzle, STAGES-deep ring;
 //   warp 1      TMEM owner and tcgen05.mma issuer (converged warp, one
 //               elected lane per instruction)
 //               (M 128, N BN, K 16), two accumulators 256 columns apart;
@@ -46,7 +47,11 @@ struct ConvTcParams {
   int G;            // groups (channels C_out / G each)
 };
 
-constexpr int kThreads = 192;
+// warps 0 and 6 produce (alternate stages), warp 1 issues MMAs, warps 2..5
+// convert: one thread issuing every copy could not keep up with 320 MMA
+// cycles per stage, and a second issuing warp nearly doubles the copy rate
+constexpr int kProducers = 2;
+constexpr int kThreads = 192 + 32 * (kProducers - 1);
 constexpr int BM = 128, BK = 64;
 
 // Butterfly reduce-scatter over the warp: lane l ends with the sum over all
@@ -124,7 +129,8 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   const int tiles = p.m_tiles * p.n_tiles;
   const int Hp = p.H / p.P;
 
-  if (warp == 0) {
+  if (warp == 0 || warp >= 6) {
+    const int pid = warp == 0 ? 0 : warp - 5;  // this producer's stages: stage % kProducers
     {  // ------------------------- TMA producer (converged warp, elected lane)
       int stage = 0;
       uint32_t phase = 0;
@@ -144,6 +150,13 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           const int hc = (p.zero_halo && halo_row) ? -1 : hh;
           const int ww = w0 + tap % 3 - 1;
           const CUtensorMap *src = (p.use_stale && halo_row) ? &tmS : &tmX;
+          if (stage % kProducers != pid) {  // another producer warp's stage
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
           uint8_t *sa = smem + stage * STAGE_BYTES;
           mbar_arrive_expect_tx_w(&full[stage], STAGE_BYTES);
