@@ -16,9 +16,11 @@
 //               to 16, K and V planes} into one of two slots; each Q tile
 //               {64 channels, 128 queries} into a 4-deep ring;
 //   warp 1      TMEM owner and MMA issuer: S_i = Q_i K^T (M 128, N keys
-//               rounded to 16, K 64) into one of two TMEM buffers, and once
-//               the softmax has written P_i, O_i = P_i V (M 128, N 64, K keys;
-//               P from TMEM, V MN-major from shared memory);
+//               rounded to 16, K 64) into TMEM buffer i mod NB once that
+//               buffer's previous tile is out, and once the softmax has
+//               written P_i, O_i = P_i V (M 128, N 64, K keys; P from TMEM,
+//               V MN-major from shared memory), each group of instructions
+//               issued by one elected lane;
 //   warps 2..   NB groups of four warps (NB = 3 when the keys round up to at
 //               most 96, else 2), one per TMEM buffer, taking the tiles in
 //               turn; one thread per query row: S row from TMEM (read twice:
