@@ -498,12 +498,18 @@ class Step:
         self.row_bytes = c_.W * c_.C * 2
         self.ops = ["conv", "groupnorm", "self_attn", "cross_attn", "cfg", "refresh"]
 
-    def run(self, events=None, core_events=None):
-        """One displaced step; events (len 7) bracket the six ABI calls."""
+    def run(self, events=None, core_events=None, waits=None):
+        """One displaced step; events (len 7) bracket the six ABI calls;
+        waits maps a call's index (0 conv, 2 self-attention, 4 guidance) to
+        an event the stream waits for before that call (its input copied
+        in)."""
         dpp, s, w = self.dpp, self.stream, self.w
         c = w.conv
         k0, k1 = self.i % 2, (self.i + 1) % 2
         rec = (lambda j: events[j].record(s)) if events else (lambda j: None)
+        pre = (lambda j: s.wait_event(waits[j]) if j in waits else None) if waits else \
+            (lambda j: None)
+        pre(0)
         rec(0)
         # conv whose epilogue also sums each band of its output for the GroupNorm
         dpp.dpp_conv3x3_gn(self.conv_desc, self.x, self.stale, self.wconv, None, self.y1,
@@ -512,6 +518,7 @@ class Step:
         dpp.dpp_groupnorm_apply(self.gn_desc, self.y1, self.stats[k0], self.gn_sums,
                                 self.stats[k1], self.gamma, self.beta, self.y2, stream=s)
         rec(2)
+        pre(2)
         if core_events:
             dpp.dpp_set_attn_core_events(*core_events)
         dpp.dpp_self_attn(self.attn_desc, self.xa, self.aw["wq"], self.aw["wk"], self.aw["wv"],
@@ -524,6 +531,7 @@ class Step:
             dpp.dpp_cross_attn_cached(self.cross_desc, self.ya, self.kv_ctx, self.xw["wq"],
                                       self.xw["wo"], self.yc, self.xa_ws, self.xa_ws_n, stream=s)
         rec(4)
+        pre(4)
         if self.has_cfg:
             dpp.dpp_cfg_combine(self.u, self.c, w.cfg_scale, self.n_cfg, self.cfg_out,
                                 self.sums, self.cfg_ws, self.cfg_ws_n, stream=s)
@@ -558,12 +566,21 @@ class Step:
         for n, t in self._sets[i].items():
             setattr(self, n, t)
 
-    def h2d(self, stream):
+    def h2d(self, stream, marks=None):
+        """Copies the step's inputs in; marks (3 events), if given, are
+        recorded after the conv input, the attention input and the guidance
+        maps."""
         with torch.cuda.stream(stream):
             self.x.copy_(self.host_x, non_blocking=True)
+            if marks:
+                marks[0].record(stream)
             self.xa.copy_(self.host_xa, non_blocking=True)
+            if marks:
+                marks[1].record(stream)
             self.u.copy_(self.host_u, non_blocking=True)
             self.c.copy_(self.host_c, non_blocking=True)
+            if marks:
+                marks[2].record(stream)
         return sum(t.numel() * t.element_size() for t in
                    (self.host_x, self.host_xa, self.host_u, self.host_c))
 
@@ -572,9 +589,15 @@ class Step:
                          for t in (self.y2, self.yc, self.cfg_out, self.sums)]
         return sum(t.numel() * t.element_size() for t in self.out_host)
 
-    def d2h(self, stream):
+    def d2h(self, stream, after=None):
+        """Copies the step's results out; after (3 events), if given, are
+        waited for before the GroupNorm output, the cross-attention output
+        and the guidance results respectively."""
         with torch.cuda.stream(stream):
-            for h, d in zip(self.out_host, (self.y2, self.yc, self.cfg_out, self.sums)):
+            for k, (h, d) in enumerate(zip(self.out_host,
+                                           (self.y2, self.yc, self.cfg_out, self.sums))):
+                if after and k < 3:
+                    stream.wait_event(after[k])
                 h.copy_(d, non_blocking=True)
 
 
@@ -925,12 +948,15 @@ def main():
         # copies of one step overlap the other set's compute, and the two
         # directions run on two copy streams (PCIe is full duplex: one stream
         # would serialise them): step k+1's inputs are copied in once step
-        # k-1, the last reader of that set, is done; step k's results are
-        # copied out once step k is done; step k+2 overwrites step k's result
-        # buffers only after they are copied out.
+        # k-1, the last reader of that set, is done; each op of a step starts
+        # once its own input has landed, and each result is copied out as
+        # soon as its op is done (the GroupNorm output while the attention
+        # runs); step k+2 overwrites step k's result buffers only after they
+        # are copied out.
         step.make_io_sets()
         cs_in, cs_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        in_ready = [torch.cuda.Event() for _ in range(2)]
+        marks = [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]  # inputs landed
+        op_ev = [[torch.cuda.Event() for _ in range(7)] for _ in range(2)]  # ops done
         done = [torch.cuda.Event() for _ in range(2)]
         out_done = [torch.cuda.Event() for _ in range(2)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -938,8 +964,7 @@ def main():
         cs_out.wait_stream(s)
         e0.record(cs_in)
         step.select(0)
-        bi = step.h2d(cs_in)
-        in_ready[0].record(cs_in)
+        bi = step.h2d(cs_in, marks[0])
         # The sampler's side of each step: once a step's results are on the
         # host, its discrepancy (rel-MAE from the guidance sums) goes to the
         # adaptive switching controller, which names the stage of the steps
@@ -957,10 +982,9 @@ def main():
         for k in range(K):
             i, j = k % 2, 1 - k % 2
             step.select(i)
-            s.wait_event(in_ready[i])
             if k >= 2:
                 s.wait_event(out_done[i])  # step k-2's results are out of this set
-            step.run()
+            step.run(events=op_ev[i], waits={0: marks[i][0], 2: marks[i][1], 4: marks[i][2]})
             done[i].record(s)
             if k >= 1:
                 observe(k - 1)
@@ -968,11 +992,9 @@ def main():
                 if k >= 1:
                     cs_in.wait_event(done[j])
                 step.select(j)
-                step.h2d(cs_in)
-                in_ready[j].record(cs_in)
+                step.h2d(cs_in, marks[j])
                 step.select(i)
-            cs_out.wait_event(done[i])
-            step.d2h(cs_out)
+            step.d2h(cs_out, (op_ev[i][2], op_ev[i][4], op_ev[i][5]))
             out_done[i].record(cs_out)
         observe(K - 1)
         cs_out.wait_stream(cs_in)
