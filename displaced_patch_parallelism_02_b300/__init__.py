@@ -117,6 +117,11 @@ _SIGNATURES = {
                                   _vp, _vp]),
     "dpp_groupnorm_static": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp, _vp, _vp, _vp,
                                    _vp]),
+    "dpp_groupnorm_sums": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp]),
+    "dpp_groupnorm_affine": (_st, [ctypes.POINTER(dpp_gn_desc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                   _vp]),
+    "dpp_conv3x3_norm": (_st, [ctypes.POINTER(dpp_conv_desc), _vp, _vp, _vp, _vp, ctypes.c_int,
+                               _vp, _vp, _vp, ctypes.c_int, _vp, _vp]),
     "dpp_self_attn": (_st, [ctypes.POINTER(dpp_attn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _vp, _sz, _vp]),
     "dpp_self_attn_workspace_bytes": (_sz, [ctypes.POINTER(dpp_attn_desc)]),
@@ -130,6 +135,7 @@ _SIGNATURES = {
     "dpp_cfg_combine": (_st, [_vp, _vp, ctypes.c_float, _sz, _vp, _vp, _vp, _sz, _vp]),
     "dpp_cfg_workspace_bytes": (_sz, [_sz]),
     "dpp_refresh_stale": (_st, [_vp, _vp, _sz, _sz, _sz, ctypes.c_int, ctypes.c_uint64, _vp]),
+    "dpp_refresh_halo": (_st, [_vp, _vp, _sz, _sz, _sz, ctypes.c_int, _vp]),
     "dpp_device_status": (_st, [_vp]),
     "dpp_status_string": (ctypes.c_char_p, [_st]),
     "dpp_version": (ctypes.c_int, []),
@@ -234,6 +240,31 @@ def dpp_groupnorm_apply(desc: dpp_gn_desc, x, stats_prev, gn_sums, stats_next, g
                                           _ptr(gn_sums), _ptr(stats_next), _ptr(gamma),
                                           _ptr(beta), _ptr(y), _stream(stream)),
                   "dpp_groupnorm_apply", raise_on_error)
+
+
+def dpp_groupnorm_sums(desc: dpp_gn_desc, x, gn_sums, stream=None,
+                       raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_groupnorm_sums(ctypes.byref(desc), _ptr(x), _ptr(gn_sums),
+                                         _stream(stream)),
+                  "dpp_groupnorm_sums", raise_on_error)
+
+
+def dpp_groupnorm_affine(desc: dpp_gn_desc, gn_sums, stats_prev, stats_next, gamma, beta,
+                         affine, stream=None, raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_groupnorm_affine(ctypes.byref(desc), _ptr(gn_sums), _ptr(stats_prev),
+                                           _ptr(stats_next), _ptr(gamma), _ptr(beta),
+                                           _ptr(affine), _stream(stream)),
+                  "dpp_groupnorm_affine", raise_on_error)
+
+
+def dpp_conv3x3_norm(desc: dpp_conv_desc, x, stale_prev, affine, affine_prev, act: int, w, bias,
+                     y, G: int = 0, gn_sums=None, stream=None,
+                     raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_conv3x3_norm(ctypes.byref(desc), _ptr(x), _ptr(stale_prev),
+                                       _ptr(affine), _ptr(affine_prev), int(act), _ptr(w),
+                                       _ptr(bias), _ptr(y), int(G), _ptr(gn_sums),
+                                       _stream(stream)),
+                  "dpp_conv3x3_norm", raise_on_error)
 
 
 def dpp_wait_selftest(kind: int, scratch=None, stream=None, raise_on_error: bool = True) -> int:
@@ -351,6 +382,13 @@ def dpp_refresh_stale(fresh, stale, outer: int, rows: int, row_bytes: int, P: in
                                         int(row_bytes), int(P), int(patch_mask) & ((1 << 64) - 1),
                                         _stream(stream)),
                   "dpp_refresh_stale", raise_on_error)
+
+
+def dpp_refresh_halo(fresh, stale, outer: int, rows: int, row_bytes: int, P: int, stream=None,
+                     raise_on_error: bool = True) -> int:
+    return _check(lib.dpp_refresh_halo(_ptr(fresh), _ptr(stale), int(outer), int(rows),
+                                       int(row_bytes), int(P), _stream(stream)),
+                  "dpp_refresh_halo", raise_on_error)
 
 
 __all__ = [n for n in dir() if n.startswith(("dpp_", "DPP_"))] + ["DppError", "lib", "LIB_PATH"]

@@ -7,10 +7,10 @@ buffers); the layers DistriFusion replaces (convolutions, GroupNorms, self-
 attention) read the previous step's state of the other bands, the per-token
 layers (LayerNorm, projections, the gated feed-forward) need none:
 
-  ResNet block   g1 = SiLU(GN1(x))              dpp_groupnorm (act SiLU)
-                 h1 = conv1(g1) + b1            dpp_conv3x3_gn (sums for GN2)
-                 g2 = SiLU(GN2(h1))             dpp_groupnorm_apply (act SiLU)
-                 x += conv2(g2) + b2            dpp_conv3x3_gn (accumulate; sums for GN)
+  ResNet block   h1 = conv1(SiLU(GN1(x))) + b1  dpp_groupnorm_sums + dpp_groupnorm_affine,
+                                                dpp_conv3x3_norm (sums for GN2)
+                 x += conv2(SiLU(GN2(h1))) + b2 dpp_groupnorm_affine (conv1's sums),
+                                                dpp_conv3x3_norm (accumulate; sums for GN)
   transformer    g = GN(x)                      dpp_groupnorm_apply
                  h = g Wpi^T + bpi              dpp_linear
                  h += attn1(LN1(h))             dpp_layernorm, dpp_self_attn (accumulate)
@@ -18,10 +18,18 @@ layers (LayerNorm, projections, the gated feed-forward) need none:
                  h += GEGLU(LN3(h)) W2^T + b2   dpp_layernorm, dpp_linear (GEGLU), dpp_linear
                  x += h Wpo^T + bpo             dpp_linear (accumulate)
 
+The ResNet block's GroupNorms are reduced to a scale and shift per band,
+image and channel that the following conv applies (with the SiLU) as it loads
+its input, so the normalised tensors are never stored; with fuse_norm=False
+they are (dpp_groupnorm / dpp_groupnorm_apply with act SiLU, then
+dpp_conv3x3_gn), which gives the same results up to rounding.
+
 The chain runs in place on x (the residual stream).  On one GPU every band's
 fresh activations of step t are all in HBM, so the stale state of step t+1 is
-simply step t's fresh buffer: the conv inputs, GroupNorm partials and K/V
-state are double-buffered and swapped each step (the refresh costs nothing).
+simply step t's fresh buffer: the conv inputs, GroupNorm partials and affines
+and the K/V state are double-buffered and swapped each step (the refresh costs
+nothing).  x itself is overwritten later in the step, so for conv1 only the
+rows the next step reads as halo are kept (dpp_refresh_halo).
 The time embedding is the same for both images of a guidance pair, so it is
 part of conv1's bias.
 """
@@ -30,10 +38,11 @@ from __future__ import annotations
 import torch
 
 from . import (DPP_ACT_SILU, DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_attn_desc,
-               dpp_conv3x3_gn, dpp_conv_desc, dpp_cross_attn, dpp_cross_attn_workspace_bytes,
-               dpp_gn_desc, dpp_groupnorm, dpp_groupnorm_apply, dpp_groupnorm_workspace_bytes,
-               dpp_layernorm, dpp_linear, dpp_linear_desc, dpp_ln_desc, dpp_self_attn,
-               dpp_self_attn_workspace_bytes)
+               dpp_conv3x3_gn, dpp_conv3x3_norm, dpp_conv_desc, dpp_cross_attn,
+               dpp_cross_attn_workspace_bytes, dpp_gn_desc, dpp_groupnorm, dpp_groupnorm_affine,
+               dpp_groupnorm_apply, dpp_groupnorm_sums, dpp_groupnorm_workspace_bytes,
+               dpp_layernorm, dpp_linear, dpp_linear_desc, dpp_ln_desc, dpp_refresh_halo,
+               dpp_self_attn, dpp_self_attn_workspace_bytes)
 
 # weight names (torch layouts: conv [C, C, 3, 3] is passed channels-last,
 # i.e. [C, 3, 3, C]; Linear [out, in]; biases and affines fp32)
@@ -90,8 +99,9 @@ class BlockChain:
     affines); ff1_w is [2 F, C] (value rows, then gate rows), ff2_w [C, F]."""
 
     def __init__(self, B, H, W, C, heads, P, G, n_ctx, c_ctx, weights, device,
-                 ff_mult=4, eps_gn_res=1e-5, eps_gn_tf=1e-6, eps_ln=1e-5):
+                 ff_mult=4, eps_gn_res=1e-5, eps_gn_tf=1e-6, eps_ln=1e-5, fuse_norm=True):
         self.B, self.H, self.W, self.C, self.P, self.G = B, H, W, C, P, G
+        self.fuse_norm = bool(fuse_norm)
         self.heads, self.n_ctx, self.c_ctx, self.F = heads, n_ctx, c_ctx, ff_mult * C
         dev = full_device(device)
         self.dev = dev
@@ -101,9 +111,19 @@ class BlockChain:
         self.M = M
         act = lambda *s: torch.empty(s, dtype=bf, device=dev)
         img = (B, H, W, C)
-        self.g1 = [act(*img), act(*img)]   # conv1 input: fresh / previous step's
-        self.g2 = [act(*img), act(*img)]   # conv2 input
-        self.h1 = act(*img)
+        if self.fuse_norm:
+            # conv1 reads x; of the previous step's x only the halo rows
+            self.xh = [torch.zeros(img, dtype=bf, device=dev) for _ in range(2)]
+            self.h1 = [act(*img), act(*img)]  # conv1 output = conv2 input, raw
+            aff = lambda: [torch.empty((P, B, C, 2), dtype=torch.float32, device=dev)
+                           for _ in range(2)]
+            self.aff1, self.aff2 = aff(), aff()
+            Hp = H // P
+            self.halo_rows = sorted({r for k in range(1, P) for r in (k * Hp - 1, k * Hp)})
+        else:
+            self.g1 = [act(*img), act(*img)]   # conv1 input: fresh / previous step's
+            self.g2 = [act(*img), act(*img)]   # conv2 input
+            self.h1 = act(*img)
         self.gt = act(B, N, C)             # transformer GroupNorm output
         self.h = act(B, N, C)              # transformer residual stream
         self.t = act(B, N, C)              # LayerNorm output
@@ -112,7 +132,7 @@ class BlockChain:
                          for _ in range(2)]
         self.st1, self.st2, self.stt = stats(), stats(), stats()
         self.sums = [torch.empty((P, B, G, 2), dtype=torch.float64, device=dev)
-                     for _ in range(2)]
+                     for _ in range(3)]
         self.kv = [torch.empty((B, N, 2, C), dtype=torch.float16, device=dev) for _ in range(2)]
         self.gn1 = dpp_gn_desc(B, H, W, C, G, P, eps_gn_res, DPP_BF16, 0, DPP_ACT_SILU)
         self.gn2 = dpp_gn_desc(B, H, W, C, G, P, eps_gn_res, DPP_BF16, 0, DPP_ACT_SILU)
@@ -145,7 +165,18 @@ class BlockChain:
         return conv + lin + self_attn + cross
 
     # the displaced states a step publishes for the next one to read
-    STATES = ("g1", "g2", "st1", "st2", "stt", "kv")
+    STATES_FUSED = ("xh", "h1", "aff1", "aff2", "st1", "st2", "stt", "kv")
+    STATES_UNFUSED = ("g1", "g2", "st1", "st2", "stt", "kv")
+
+    @property
+    def STATES(self):
+        return self.STATES_FUSED if self.fuse_norm else self.STATES_UNFUSED
+
+    def _state(self, name, i):
+        """The part of state buffer i the next step reads (of x's copy: the
+        halo rows)."""
+        t = getattr(self, name)[i]
+        return t[:, self.halo_rows] if name == "xh" else t
 
     def state_dict(self):
         """A checkpoint: the step count and the states the next step reads as
@@ -159,7 +190,7 @@ class BlockChain:
         i = (self.k - 1) % 2  # the buffers the last step wrote
         torch.cuda.synchronize(self.dev)
         for name in self.STATES:
-            sd[name] = getattr(self, name)[i].cpu()
+            sd[name] = self._state(name, i).cpu()
         return sd
 
     def load_state_dict(self, sd):
@@ -170,11 +201,17 @@ class BlockChain:
         if k > 0:
             i = (k - 1) % 2
             for name in self.STATES:
-                dst, src = getattr(self, name)[i], sd[name]
+                if name not in sd:
+                    raise ValueError(f"{name}: not in the checkpoint (a chain with "
+                                     f"fuse_norm={not self.fuse_norm}?)")
+                dst, src = self._state(name, i), sd[name]
                 if tuple(src.shape) != tuple(dst.shape) or src.dtype != dst.dtype:
                     raise ValueError(f"{name}: checkpoint {tuple(src.shape)} {src.dtype}, "
                                      f"chain {tuple(dst.shape)} {dst.dtype}")
-                dst.copy_(src)
+                if name == "xh":
+                    getattr(self, name)[i][:, self.halo_rows] = src.to(self.dev)
+                else:
+                    dst.copy_(src)
         self.k = k
 
     def step(self, x, ctx, stream=None, hook=None):
@@ -189,6 +226,7 @@ class BlockChain:
                 raise ValueError(f"{name}: want {shape} bf16 contiguous on {self.dev}, got "
                                  f"{tuple(t.shape)} {t.dtype} on {t.device}")
         w, s = self.w, stream
+        self._s = stream
         i, j = self.k % 2, 1 - self.k % 2
         first = self.k == 0
         prev = (lambda a: None) if first else (lambda a: a[j])
@@ -202,6 +240,50 @@ class BlockChain:
             call(name, "post", dict(ins, out=out))
 
         # ---------------------------------------------------------- ResNet block
+        if self.fuse_norm:
+            self._resnet_fused(x, i, prev, op)
+        else:
+            self._resnet_unfused(x, i, prev, op)
+        # ------------------------------------------------------ transformer block
+        op("gn", lambda: dpp_groupnorm_apply(self.gnt, x, prev(self.stt), self.sums[1],
+                                             self.stt[i], w["gn_g"], w["gn_b"], self.gt,
+                                             stream=s),
+           {"x": x}, self.gt)
+        self._transformer(x, tok, ctx, i, prev, op)
+        self.k += 1
+
+    def _resnet_fused(self, x, i, prev, op):
+        """GroupNorm -> SiLU folded into the convs' loads.  gn1: the band sums
+        of x, its affine, and x's halo rows kept for the next step's conv1
+        (before conv2 overwrites x); gn2: the affine of conv1's epilogue
+        sums."""
+        w, s, B, H, W, C, P = self.w, self._s, self.B, self.H, self.W, self.C, self.P
+
+        def gn1():
+            dpp_groupnorm_sums(self.gn1, x, self.sums[2], stream=s)
+            dpp_groupnorm_affine(self.gn1, self.sums[2], prev(self.st1), self.st1[i],
+                                 w["gn1_g"], w["gn1_b"], self.aff1[i], stream=s)
+            dpp_refresh_halo(x, self.xh[i], B, H, W * C * 2, P, stream=s)
+
+        op("gn1", gn1, {"x": x}, self.aff1[i])
+        op("conv1", lambda: dpp_conv3x3_norm(self.conv1, x, prev(self.xh), self.aff1[i],
+                                             prev(self.aff1), DPP_ACT_SILU, w["conv1_w"],
+                                             w["conv1_b"], self.h1[i], self.G, self.sums[0],
+                                             stream=s),
+           {"x": x}, self.h1[i])
+        op("gn2", lambda: dpp_groupnorm_affine(self.gn2, self.sums[0], prev(self.st2),
+                                               self.st2[i], w["gn2_g"], w["gn2_b"],
+                                               self.aff2[i], stream=s),
+           {"x": self.h1[i]}, self.aff2[i])
+        op("conv2", lambda: dpp_conv3x3_norm(self.conv2, self.h1[i], prev(self.h1),
+                                             self.aff2[i], prev(self.aff2), DPP_ACT_SILU,
+                                             w["conv2_w"], w["conv2_b"], x, self.G, self.sums[1],
+                                             stream=s),
+           {"x": self.h1[i]}, x)
+
+    def _resnet_unfused(self, x, i, prev, op):
+        """GroupNorm -> SiLU stored, then read by the conv."""
+        w, s = self.w, self._s
         op("gn1", lambda: dpp_groupnorm(self.gn1, x, prev(self.st1), self.st1[i], w["gn1_g"],
                                         w["gn1_b"], self.g1[i], self.gn_ws, self.gn_ws_n,
                                         stream=s),
@@ -217,11 +299,9 @@ class BlockChain:
         op("conv2", lambda: dpp_conv3x3_gn(self.conv2, self.g2[i], prev(self.g2), w["conv2_w"],
                                            w["conv2_b"], x, self.G, self.sums[1], stream=s),
            {"x": self.g2[i]}, x)
-        # ------------------------------------------------------ transformer block
-        op("gn", lambda: dpp_groupnorm_apply(self.gnt, x, prev(self.stt), self.sums[1],
-                                             self.stt[i], w["gn_g"], w["gn_b"], self.gt,
-                                             stream=s),
-           {"x": x}, self.gt)
+
+    def _transformer(self, x, tok, ctx, i, prev, op):
+        w, s = self.w, self._s
         op("proj_in", lambda: dpp_linear(self.lin, self.gt, w["pi_w"], w["pi_b"], self.h,
                                          stream=s),
            {"x": self.gt}, self.h)
@@ -250,7 +330,6 @@ class BlockChain:
         op("proj_out", lambda: dpp_linear(self.lin_acc, self.h, w["po_w"], w["po_b"], tok,
                                           stream=s),
            {"x": self.h}, tok)
-        self.k += 1
 
 
 class BranchPair:

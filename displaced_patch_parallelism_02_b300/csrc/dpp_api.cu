@@ -238,6 +238,21 @@ dpp_status dpp_refresh_stale(const void *fresh, void *stale, size_t outer, size_
                                           (cudaStream_t)stream), 1));
 }
 
+dpp_status dpp_refresh_halo(const void *fresh, void *stale, size_t outer, size_t rows,
+                            size_t row_bytes, int P, dpp_stream stream) {
+  if (!fresh || !stale) return DPP_ERR_INVALID_ARG;
+  if (P < 1 || rows == 0 || outer == 0 || rows % (size_t)P) return DPP_ERR_INVALID_ARG;
+  if (row_bytes == 0 || row_bytes % 16) return DPP_ERR_INVALID_ARG;
+  if (!aligned16(fresh) || !aligned16(stale)) return DPP_ERR_ALIGN;
+  const size_t total = outer * rows * row_bytes;
+  if (total / outer / rows != row_bytes) return DPP_ERR_INVALID_ARG;  // overflow
+  if (overlap(fresh, total, stale, total)) return DPP_ERR_ALIAS;
+  if (P == 1) return DPP_OK;  // one band: no halo
+  if (outer * 2 * (size_t)(P - 1) > 65535) return DPP_ERR_UNSUPPORTED;
+  return from_cuda(counted(
+      launch_refresh_halo(fresh, stale, outer, rows, row_bytes, P, (cudaStream_t)stream), 1));
+}
+
 // ---------------------------------------------------------------------- CFG
 size_t dpp_cfg_workspace_bytes(size_t n) { return 16 + cfg_blocks(n) * 3 * sizeof(double); }
 
@@ -366,6 +381,78 @@ dpp_status dpp_groupnorm_apply(const dpp_gn_desc *d, const void *x, const float 
   return from_cuda(counted(launch_groupnorm_apply(*d, x, stats_prev, gn_sums, stats_next, gamma,
                                                   beta, y, (cudaStream_t)stream),
                            1));
+}
+
+// ------------------------------- GroupNorm -> SiLU applied on the conv's load
+dpp_status dpp_groupnorm_sums(const dpp_gn_desc *d, const void *x, double *gn_sums,
+                              dpp_stream stream) {
+  dpp_status st = check_gn(d);
+  if (st != DPP_OK) return st;
+  if (!x || !gn_sums) return DPP_ERR_INVALID_ARG;
+  if (d->G > 1024 || d->C / chan_quantum(d->dtype) > 512) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(gn_sums)) return DPP_ERR_ALIGN;
+  const size_t nx = (size_t)d->B * d->H * d->W * d->C * elem_size(d->dtype);
+  if (overlap(gn_sums, (size_t)d->P * d->B * d->G * 2 * sizeof(double), x, nx))
+    return DPP_ERR_ALIAS;
+  return from_cuda(counted(launch_groupnorm_sums(*d, x, gn_sums, (cudaStream_t)stream), 2));
+}
+
+dpp_status dpp_groupnorm_affine(const dpp_gn_desc *d, const double *gn_sums,
+                                const float *stats_prev, float *stats_next, const float *gamma,
+                                const float *beta, float *affine, dpp_stream stream) {
+  dpp_status st = check_gn(d);
+  if (st != DPP_OK) return st;
+  if (!gn_sums || !affine) return DPP_ERR_INVALID_ARG;
+  if ((gamma == nullptr) != (beta == nullptr)) return DPP_ERR_INVALID_ARG;
+  if (d->G > 1024) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(gn_sums) || !aligned16(affine) || (stats_next && !aligned16(stats_next)) ||
+      (stats_prev && !aligned16(stats_prev)))
+    return DPP_ERR_ALIGN;
+  const size_t ns = (size_t)d->P * d->B * d->G * 2 * sizeof(float);
+  const size_t na = (size_t)d->P * d->B * d->C * 2 * sizeof(float);
+  if (overlap(affine, na, gn_sums, 2 * ns) || overlap(affine, na, stats_prev, ns) ||
+      overlap(affine, na, stats_next, ns) || overlap(affine, na, gamma, d->C * sizeof(float)) ||
+      overlap(affine, na, beta, d->C * sizeof(float)) || overlap(stats_next, ns, gn_sums, 2 * ns) ||
+      overlap(stats_next, ns, stats_prev, ns))
+    return DPP_ERR_ALIAS;
+  return from_cuda(counted(launch_groupnorm_affine(*d, gn_sums, stats_prev, stats_next, gamma,
+                                                   beta, affine, (cudaStream_t)stream),
+                           1));
+}
+
+dpp_status dpp_conv3x3_norm(const dpp_conv_desc *d, const void *x, const void *stale_prev,
+                            const float *affine, const float *affine_prev, int act,
+                            const void *w, const float *bias, void *y, int G, double *gn_sums,
+                            dpp_stream stream) {
+  dpp_status st = check_conv(d, x, stale_prev, w, bias, y);
+  if (st != DPP_OK) return st;
+  if (!affine || (act != DPP_ACT_NONE && act != DPP_ACT_SILU)) return DPP_ERR_INVALID_ARG;
+  const bool use_stale = stale_prev && stale_prev != x && d->halo == DPP_HALO_STALE;
+  if (use_stale && !affine_prev) return DPP_ERR_INVALID_ARG;
+  if (gn_sums && (G < 1 || d->C_out % G)) return DPP_ERR_INVALID_ARG;
+  if (!conv_tc_supported(*d)) return DPP_ERR_UNSUPPORTED;
+  if (!aligned16(affine) || (affine_prev && !aligned16(affine_prev)) ||
+      (gn_sums && !aligned16(gn_sums)))
+    return DPP_ERR_ALIGN;
+  const size_t es = elem_size(d->dtype);
+  const long long pix = (long long)d->B * d->H * d->W;
+  const size_t ny = (size_t)pix * d->C_out * es;
+  const size_t na = (size_t)d->P * d->B * d->C_in * 2 * sizeof(float);
+  if (overlap(y, ny, affine, na) || (use_stale && overlap(y, ny, affine_prev, na)))
+    return DPP_ERR_ALIAS;
+  if (gn_sums) {
+    const size_t ns = (size_t)d->P * d->B * G * 2 * sizeof(double);
+    if (overlap(gn_sums, ns, y, ny) || overlap(gn_sums, ns, x, (size_t)pix * d->C_in * es) ||
+        overlap(gn_sums, ns, stale_prev, (size_t)pix * d->C_in * es) ||
+        overlap(gn_sums, ns, w, (size_t)d->C_out * 9 * d->C_in * es) ||
+        overlap(gn_sums, ns, bias, (size_t)d->C_out * sizeof(float)) ||
+        overlap(gn_sums, ns, affine, na) || (use_stale && overlap(gn_sums, ns, affine_prev, na)))
+      return DPP_ERR_ALIAS;
+  }
+  return from_cuda(counted(
+      launch_conv_norm_tc(*d, x, stale_prev, affine, use_stale ? affine_prev : nullptr, act, w,
+                          bias, y, device_status_ptr(), (cudaStream_t)stream, gn_sums, G),
+      gn_sums ? 2 : 1));
 }
 
 // ---------------------------------------------------------------- attention

@@ -26,6 +26,9 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // refresh: copy selected bands of [outer][rows][row_bytes] (row_bytes % 16 == 0)
 cudaError_t launch_refresh(const void *fresh, void *stale, size_t outer, size_t rows,
                            size_t row_bytes, int P, uint64_t mask, cudaStream_t s);
+// halo refresh: at each band boundary the two rows beside it (P >= 2)
+cudaError_t launch_refresh_halo(const void *fresh, void *stale, size_t outer, size_t rows,
+                                size_t row_bytes, int P, cudaStream_t s);
 
 // guidance combine + discrepancy sums
 size_t cfg_blocks(size_t n);
@@ -46,6 +49,15 @@ cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *s
 cudaError_t launch_groupnorm_apply(const dpp_gn_desc &d, const void *x, const float *stats_prev,
                                    const double *gn_sums, float *stats_next, const float *gamma,
                                    const float *beta, void *y, cudaStream_t s);
+// The band sums of x in a pass of their own (gn_sums fp64 [P][B][G][2],
+// zeroed first), and the per-band affine (a, s) [P][B][C][2] fp32 that the
+// normalising conv applies, with stats_next[p] = gn_sums[p] in fp32.
+cudaError_t launch_groupnorm_sums(const dpp_gn_desc &d, const void *x, double *gn_sums,
+                                  cudaStream_t s);
+cudaError_t launch_groupnorm_affine(const dpp_gn_desc &d, const double *gn_sums,
+                                    const float *stats_prev, float *stats_next,
+                                    const float *gamma, const float *beta, float *affine,
+                                    cudaStream_t s);
 
 // GroupNorm with its scratch in a static device array of this many bytes
 // (no workspace argument, no allocation).
@@ -66,6 +78,15 @@ bool conv_tc_supported(const dpp_conv_desc &d);
 cudaError_t launch_conv_tc(const dpp_conv_desc &d, const void *x, const void *stale,
                            const void *w, const float *bias, void *y, int *status,
                            cudaStream_t s, double *gn_sums = nullptr, int G = 0);
+// The same conv reading act(x * a + s) (GroupNorm -> SiLU applied on load):
+// affine / affine_prev [P][B][C_in][2] fp32 (scale, shift) per band of the
+// row read, of this step and of the previous one (halo rows from stale).
+cudaError_t launch_conv_norm_tc(const dpp_conv_desc &d, const void *x, const void *stale,
+                                const float *affine, const float *affine_prev, int act,
+                                const void *w, const float *bias, void *y, int *status,
+                                cudaStream_t s, double *gn_sums = nullptr, int G = 0);
+// zero n doubles (the fp64 totals the sum kernels add into)
+cudaError_t launch_zero_f64(double *p, size_t n, cudaStream_t s);
 
 // Element types inside the library.  Attention layers whose activations are
 // bf16 keep Q, O and the K/V state in fp16: the same tensor-core rate with

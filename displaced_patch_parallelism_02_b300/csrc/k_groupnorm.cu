@@ -614,6 +614,36 @@ cudaError_t launch_groupnorm(const dpp_gn_desc &d, const void *x, const float *s
 namespace dpp {
 namespace {
 
+// Band p's statistics of image b and group g: its fresh sums gn_sums[p] plus
+// the other bands' stale partials stats_prev[q] (every band's fresh sums in
+// the synchronous step, stats_prev == NULL; the band's own alone when
+// band_local), in fp64; mean and 1/sqrt(var + eps) rounded to fp32.
+__device__ __forceinline__ void gn_band_stats(const double *__restrict__ gn_sums,
+                                              const float *__restrict__ stats_prev, int B, int H,
+                                              int W, int cg, int G, int P, int band_local, int p,
+                                              int b, int g, float eps, float &mean_f,
+                                              float &rstd_f) {
+  const double *fr = gn_sums + (((size_t)p * B + b) * G + g) * 2;
+  double t1 = fr[0], t2 = fr[1];
+  for (int q = 0; q < P && !band_local; ++q) {
+    if (q == p) continue;
+    if (stats_prev) {
+      const float *sq = stats_prev + (((size_t)q * B + b) * G + g) * 2;
+      t1 += sq[0];
+      t2 += sq[1];
+    } else {
+      const double *fq = gn_sums + (((size_t)q * B + b) * G + g) * 2;
+      t1 += fq[0];
+      t2 += fq[1];
+    }
+  }
+  const double n = (double)(band_local ? H / P : H) * W * cg;
+  const double mean = t1 / n;
+  const double var = fmax(t2 / n - mean * mean, 0.0);
+  mean_f = (float)mean;
+  rstd_f = (float)(1.0 / sqrt(var + (double)eps));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(512)
 gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int ppc, int band_local,
@@ -625,26 +655,10 @@ gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int 
   const int unit = blockIdx.y, b = unit / P, p = unit % P;
   const int cg = C / G, Hp = H / P;
   for (int g = threadIdx.x; g < G; g += blockDim.x) {
-    const double *fr = gn_sums + (((size_t)p * B + b) * G + g) * 2;
-    double t1 = fr[0], t2 = fr[1];
-    for (int q = 0; q < P && !band_local; ++q) {
-      if (q == p) continue;
-      if (stats_prev) {
-        const float *sq = stats_prev + (((size_t)q * B + b) * G + g) * 2;
-        t1 += sq[0];
-        t2 += sq[1];
-      } else {
-        const double *fq = gn_sums + (((size_t)q * B + b) * G + g) * 2;
-        t1 += fq[0];
-        t2 += fq[1];
-      }
-    }
-    const double n = (double)(band_local ? Hp : H) * W * cg;
-    const double mean = t1 / n;
-    const double var = fmax(t2 / n - mean * mean, 0.0);
-    mean_s[g] = (float)mean;
-    rstd_s[g] = (float)(1.0 / sqrt(var + (double)eps));
+    gn_band_stats(gn_sums, stats_prev, B, H, W, cg, G, P, band_local, p, b, g, eps, mean_s[g],
+                  rstd_s[g]);
     if (blockIdx.x == 0) {
+      const double *fr = gn_sums + (((size_t)p * B + b) * G + g) * 2;
       float *sn = stats_next + (((size_t)p * B + b) * G + g) * 2;
       sn[0] = (float)fr[0];
       sn[1] = (float)fr[1];
@@ -687,6 +701,111 @@ gn_apply_kernel(const T *x, T *y, int B, int H, int W, int C, int G, int P, int 
   }
 }
 
+// The band sums of x alone (what dpp_conv3x3_gn's epilogue produces for its
+// output), for a GroupNorm whose input no conv summed: one read of x.  A CTA
+// takes one chunk of one (batch, band) unit; thread t always holds channel
+// vector t % (C/VE) and adds its pixels' values and squares in fp32.  The
+// CTA then folds them in a fixed order -- per channel over its pixel rows,
+// per group over its channels -- and adds each group's fp32 sums into the
+// fp64 totals (zeroed by the launcher).  fp32 values of similar size add
+// exactly in fp64, so the totals do not depend on the order the CTAs' atomics
+// land in: the sums are bit-reproducible.
+template <typename T>
+__global__ void __launch_bounds__(512)
+gn_sums_kernel(const T *x, int B, int H, int W, int C, int G, int P, int ppc,
+               double *__restrict__ gn_sums) {
+  constexpr int VE = Vec16<T>::N;
+  __shared__ float part[2][512 * VE];  // [R][C] per-thread channel sums (R * C = blockDim * VE)
+  const int unit = blockIdx.y, b = unit / P, p = unit % P;
+  const int cg = C / G, Hp = H / P;
+  const int VPP = C / VE, R = blockDim.x / VPP;
+  const int v = threadIdx.x % VPP, r = threadIdx.x / VPP;
+  if (r < R) {
+    float s1[VE], s2[VE];
+#pragma unroll
+    for (int e = 0; e < VE; ++e) s1[e] = s2[e] = 0.f;
+    const int npix = Hp * W;
+    const int j0 = blockIdx.x * ppc, j1 = min(j0 + ppc, npix);
+    const size_t base = ((size_t)b * H + (size_t)p * Hp) * W;
+    for (int j = j0 + r; j < j1; j += 4 * R) {
+      uint4 raw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        raw[k] = j + k * R < j1
+                     ? *reinterpret_cast<const uint4 *>(x + (base + j + k * R) * C + v * VE)
+                     : make_uint4(0u, 0u, 0u, 0u);  // zeros add nothing
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float f[VE];
+        Vec16<T>::cvt(raw[k], f);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          s1[e] += f[e];
+          s2[e] = fmaf(f[e], f[e], s2[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < VE; ++e) {
+      part[0][r * C + v * VE + e] = s1[e];
+      part[1][r * C + v * VE + e] = s2[e];
+    }
+  }
+  __syncthreads();
+  for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {  // column ch: this thread's alone
+    float t1 = 0.f, t2 = 0.f;
+    for (int k = 0; k < R; ++k) {
+      t1 += part[0][k * C + ch];
+      t2 += part[1][k * C + ch];
+    }
+    part[0][ch] = t1;
+    part[1][ch] = t2;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    float t1 = 0.f, t2 = 0.f;
+    for (int ch = g * cg; ch < (g + 1) * cg; ++ch) {
+      t1 += part[0][ch];
+      t2 += part[1][ch];
+    }
+    double *t = gn_sums + (((size_t)p * B + b) * G + g) * 2;
+    atomicAdd(t, (double)t1);
+    atomicAdd(t + 1, (double)t2);
+  }
+}
+
+// The statistics half of a displaced GroupNorm as a per-channel affine of
+// each band: affine[p][b][c] = (a, s) with a = rstd * gamma[c] and
+// s = beta[c] - mean * a (the scale and shift gn_apply_kernel applies, in
+// the same operations), and band p's fresh sums published to stats_next[p].
+// One CTA per (batch, band) unit.
+__global__ void __launch_bounds__(256)
+gn_affine_kernel(int B, int H, int W, int C, int G, int P, int band_local,
+                 const double *__restrict__ gn_sums, const float *__restrict__ stats_prev,
+                 float *__restrict__ stats_next, const float *__restrict__ gamma,
+                 const float *__restrict__ beta, float eps, float *__restrict__ affine) {
+  __shared__ float mean_s[1024], rstd_s[1024];
+  const int unit = blockIdx.x, b = unit / P, p = unit % P;
+  const int cg = C / G;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    gn_band_stats(gn_sums, stats_prev, B, H, W, cg, G, P, band_local, p, b, g, eps, mean_s[g],
+                  rstd_s[g]);
+    if (stats_next) {
+      const double *fr = gn_sums + (((size_t)p * B + b) * G + g) * 2;
+      float *sn = stats_next + (((size_t)p * B + b) * G + g) * 2;
+      sn[0] = (float)fr[0];
+      sn[1] = (float)fr[1];
+    }
+  }
+  __syncthreads();
+  float2 *out = reinterpret_cast<float2 *>(affine) + ((size_t)p * B + b) * C;
+  for (int ch = threadIdx.x; ch < C; ch += blockDim.x) {
+    const int g = ch / cg;
+    const float a = rstd_s[g] * (gamma ? gamma[ch] : 1.f);
+    out[ch] = make_float2(a, (beta ? beta[ch] : 0.f) - mean_s[g] * a);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_groupnorm_apply(const dpp_gn_desc &d, const void *x, const float *stats_prev,
@@ -712,6 +831,44 @@ cudaError_t launch_groupnorm_apply(const dpp_gn_desc &d, const void *x, const fl
         (const float *)x, (float *)y, d.B, d.H, d.W, d.C, d.G, d.P, ppc, d.band_local ? 1 : 0,
         d.act, gn_sums, stats_prev,
         stats_next, gamma, beta, d.eps);
+  return cudaGetLastError();
+}
+
+
+cudaError_t launch_groupnorm_sums(const dpp_gn_desc &d, const void *x, double *gn_sums,
+                                  cudaStream_t s) {
+  // the kernel's per-thread sums fill [R][C] <= 512 x VE floats of shared memory
+  if (d.G > 1024 || d.C / gn_vec(d) > 512) return cudaErrorNotSupported;
+  const size_t n = (size_t)d.P * d.B * d.G * 2;
+  cudaError_t e = launch_zero_f64(gn_sums, n, s);
+  if (e != cudaSuccess) return e;
+  const int VPP = d.C / gn_vec(d), R = gn_rows(d);
+  const int threads = R * VPP;
+  const int units = d.B * d.P;
+  const int npix = (d.H / d.P) * d.W;
+  int chunks = (4 * 148 + units - 1) / units;
+  const int max_chunks = (npix + 4 * R - 1) / (4 * R);
+  if (chunks > max_chunks) chunks = max_chunks;
+  if (chunks < 1) chunks = 1;
+  const int ppc = (npix + chunks - 1) / chunks;
+  dim3 grid((unsigned)chunks, (unsigned)units);
+  if (d.dtype == DPP_BF16)
+    gn_sums_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
+        (const __nv_bfloat16 *)x, d.B, d.H, d.W, d.C, d.G, d.P, ppc, gn_sums);
+  else
+    gn_sums_kernel<float><<<grid, threads, 0, s>>>((const float *)x, d.B, d.H, d.W, d.C, d.G,
+                                                   d.P, ppc, gn_sums);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_groupnorm_affine(const dpp_gn_desc &d, const double *gn_sums,
+                                    const float *stats_prev, float *stats_next,
+                                    const float *gamma, const float *beta, float *affine,
+                                    cudaStream_t s) {
+  if (d.G > 1024) return cudaErrorNotSupported;
+  gn_affine_kernel<<<(unsigned)(d.B * d.P), 256, 0, s>>>(
+      d.B, d.H, d.W, d.C, d.G, d.P, d.band_local ? 1 : 0, gn_sums, stats_prev, stats_next, gamma,
+      beta, d.eps, affine);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,22 @@ refresh_kernel(const uint4 *__restrict__ fresh, uint4 *__restrict__ stale, size_
   for (; i < band_vec; i += stride) __stcs(dst + i, __ldcs(src + i));
 }
 
+// The rows of a displaced conv's input that another band reads as its halo:
+// at every band boundary k (1 <= k < P) the last row of band k-1 and the
+// first row of band k.  blockIdx.y walks (outer slice, boundary, side).
+__global__ void __launch_bounds__(kThreads)
+halo_kernel(const uint4 *__restrict__ fresh, uint4 *__restrict__ stale, size_t rows,
+            size_t row_vec, int Hp, int nb) {
+  const size_t seg = blockIdx.y;
+  const size_t o = seg / nb;
+  const int r = (int)(seg % nb);
+  const size_t row = (size_t)(r / 2 + 1) * Hp - 1 + (r & 1);
+  const size_t base = (o * rows + row) * row_vec;
+  for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < row_vec;
+       i += (size_t)gridDim.x * kThreads)
+    __stcs(stale + base + i, __ldcs(fresh + base + i));
+}
+
 }  // namespace
 
 cudaError_t launch_refresh(const void *fresh, void *stale, size_t outer, size_t rows,
@@ -61,6 +77,19 @@ cudaError_t launch_refresh(const void *fresh, void *stale, size_t outer, size_t 
   if (segs > 65535) return cudaErrorInvalidConfiguration;
   refresh_kernel<<<dim3(gx, (unsigned)segs), kThreads, 0, s>>>(
       (const uint4 *)fresh, (uint4 *)stale, rows * row_vec, band_vec, nsel, sel);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_refresh_halo(const void *fresh, void *stale, size_t outer, size_t rows,
+                                size_t row_bytes, int P, cudaStream_t s) {
+  if (P < 2 || outer == 0 || rows == 0 || row_bytes == 0) return cudaSuccess;
+  const int nb = 2 * (P - 1);
+  const size_t segs = outer * (size_t)nb;
+  if (segs > 65535) return cudaErrorInvalidConfiguration;
+  const size_t row_vec = row_bytes / 16;
+  const unsigned gx = (unsigned)((row_vec + kThreads - 1) / kThreads);
+  halo_kernel<<<dim3(gx, (unsigned)segs), kThreads, 0, s>>>(
+      (const uint4 *)fresh, (uint4 *)stale, rows, row_vec, (int)(rows / P), nb);
   return cudaGetLastError();
 }
 

@@ -266,6 +266,62 @@ dpp_status dpp_groupnorm_apply(const dpp_gn_desc *desc, const void *x, const flo
                                const float *beta, void *y, dpp_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * dpp_groupnorm_sums + dpp_groupnorm_affine + dpp_conv3x3_norm -- the
+ * ResNet block's GroupNorm -> SiLU -> conv (DistriFusion developer guide,
+ * sections 归一化层拆分 and 卷积层拆分) with the normalised tensor never
+ * stored: the GroupNorm is reduced to one scale and shift per band, image
+ * and channel, and the conv applies them (and the SiLU) to its input as it
+ * loads it.  Results equal dpp_groupnorm (act) followed by dpp_conv3x3 on
+ * the normalised tensor, up to floating-point rounding, when the conv's
+ * stale_prev is the previous step's un-normalised input and affine_prev
+ * the previous step's affine (then the halo rows are normalised exactly as
+ * the previous step's GroupNorm normalised them).
+ *
+ * dpp_groupnorm_sums: gn_sums[p,b,g] = (sum x, sum x^2) over band p of
+ *   image b and the C/G channels of group g (what dpp_conv3x3_gn produces
+ *   for its output), for an input no conv summed.  One read of x.
+ *   gn_sums : [P, B, G, 2] fp64 device memory, overwritten.  G <= 1024 and
+ *             C <= 4096 (bf16) / 2048 (fp32), else DPP_ERR_UNSUPPORTED.
+ *   The sums are bit-reproducible (fixed reduction order).
+ *
+ * dpp_groupnorm_affine: per band p, image b, channel c in group g,
+ *   affine[p,b,c] = (a, s),  a = gamma[c] / sqrt(var + eps),
+ *                            s = beta[c] - mean * a,
+ *   with mean and var of band p's statistics as dpp_groupnorm_apply forms
+ *   them (gn_sums[p] plus stats_prev[q] for q != p; NULL stats_prev: every
+ *   band's gn_sums, the synchronous step; band_local: band p's alone).
+ *   stats_next[p] = gn_sums[p] in fp32 (the refresh of the GroupNorm
+ *   state), or NULL to skip it.  desc->act is not used (the conv applies it).
+ *   affine : [P, B, C, 2] fp32 (scale, shift interleaved), overwritten.
+ *
+ * dpp_conv3x3_norm: dpp_conv3x3 (+ dpp_conv3x3_gn's sums when gn_sums is
+ *   not NULL) of the tensor Z' with
+ *     Z'[b,h,w,c] = act(Z[b,h,w,c] * a[q,b,c] + s[q,b,c]),  q = h / (H/P),
+ *   where (a, s) is affine for the rows of band p and for fresh halo rows,
+ *   and affine_prev (the previous step's) for halo rows read from
+ *   stale_prev; image padding and the zero halo (DPP_HALO_ZERO) stay zero.
+ *   act: DPP_ACT_NONE or DPP_ACT_SILU (x * sigmoid(x), evaluated as
+ *   h + h tanh(h), h = x/2, with a hardware tanh of about 2^-11 relative
+ *   error, below the bf16 rounding of the normalised value).
+ *   affine, affine_prev : [P, B, C_in, 2] fp32 from dpp_groupnorm_affine;
+ *                         affine_prev may be NULL when no halo row is read
+ *                         from stale_prev (stale_prev NULL or == x, or a
+ *                         fresh or zero halo).
+ *   Requires the bf16 tensor-core conv (DPP_ERR_UNSUPPORTED otherwise);
+ *   other arguments and rules as dpp_conv3x3_gn.  Only the halo rows of
+ *   stale_prev are read (see dpp_refresh_halo).
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_groupnorm_sums(const dpp_gn_desc *desc, const void *x, double *gn_sums,
+                              dpp_stream stream);
+dpp_status dpp_groupnorm_affine(const dpp_gn_desc *desc, const double *gn_sums,
+                                const float *stats_prev, float *stats_next, const float *gamma,
+                                const float *beta, float *affine, dpp_stream stream);
+dpp_status dpp_conv3x3_norm(const dpp_conv_desc *desc, const void *x, const void *stale_prev,
+                            const float *affine, const float *affine_prev, int act,
+                            const void *w, const float *bias, void *y, int G, double *gn_sums,
+                            dpp_stream stream);
+
+/* ---------------------------------------------------------------------------
  * dpp_self_attn -- DistriSelfAttentionPP (section 注意力机制拆分 of the
  * DistriFusion developer guide, attn1).  For band p:
  *   Q = x[band p] wq^T;  K/V rows of band p's tokens are x[band p] wk^T /
@@ -364,6 +420,20 @@ size_t dpp_cfg_workspace_bytes(size_t n);
  * ------------------------------------------------------------------------- */
 dpp_status dpp_refresh_stale(const void *fresh, void *stale, size_t outer, size_t rows,
                              size_t row_bytes, int P, uint64_t patch_mask, dpp_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * dpp_refresh_halo -- the part of the all_gather (same section) that a
+ * displaced 3x3 conv reads: at every band boundary the last row of the band
+ * above and the first row of the band below, copied bit-exactly from fresh
+ * to stale; every other row of stale is left untouched.  For a conv input
+ * that is overwritten later in the step (the residual stream), this keeps
+ * the rows the next step reads as halo at 2 (P - 1) rows per outer slice.
+ *   View and requirements as dpp_refresh_stale (outer = B, rows = H,
+ *   row_bytes = W*C*elem for NHWC); P = 1 copies nothing;
+ *   outer * 2 * (P - 1) <= 65535.
+ * ------------------------------------------------------------------------- */
+dpp_status dpp_refresh_halo(const void *fresh, void *stale, size_t outer, size_t rows,
+                            size_t row_bytes, int P, dpp_stream stream);
 
 /* ---------------------------------------------------------------------------
  * Per-token layers of the U-Net's transformer blocks.  The DistriFusion

@@ -172,6 +172,74 @@ def test_refresh_validation():
     assert f(A, Bp, 1, 8, 64, 4, patch_mask=0, stream=0, raise_on_error=False) == dpp.DPP_OK
 
 
+def test_refresh_halo_validation():
+    f = dpp.dpp_refresh_halo
+    assert f(A, Bp, 1, 10, 64, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+    assert f(A, Bp, 1, 8, 40, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_INVALID_ARG
+    assert f(A, A + 64, 1, 8, 64, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_ALIAS
+    assert f(A + 8, Bp, 1, 8, 64, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_ALIGN
+    assert f(A, Bp, 40000, 8, 64, 4, stream=0, raise_on_error=False) == dpp.DPP_ERR_UNSUPPORTED
+    # one band has no halo: a valid no-op that launches nothing
+    before = dpp.dpp_launch_count()
+    assert f(A, Bp, 2, 8, 64, 1, stream=0, raise_on_error=False) == dpp.DPP_OK
+    assert dpp.dpp_launch_count() == before
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(C=30), {}, dpp.DPP_ERR_INVALID_ARG),            # C % G
+    (dict(G=2048, C=2048), {}, dpp.DPP_ERR_UNSUPPORTED),   # more than 1024 groups
+    (dict(C=8192, G=32), {}, dpp.DPP_ERR_UNSUPPORTED),     # more than 512 vectors a pixel
+    ({}, dict(x=0), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(sums=0), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(sums=Bp + 8), dpp.DPP_ERR_ALIGN),
+    ({}, dict(sums=A + 64), dpp.DPP_ERR_ALIAS),            # sums inside x
+])
+def test_groupnorm_sums_validation(kw, ptrs, want):
+    p = dict(x=A, sums=Bp)
+    p.update(ptrs)
+    assert dpp.dpp_groupnorm_sums(gn(**kw), p["x"], p["sums"], stream=0,
+                                  raise_on_error=False) == want
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(H=7), {}, dpp.DPP_ERR_INVALID_ARG),             # H % P
+    ({}, dict(sums=0), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(affine=0), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(gamma=Cp, beta=None), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(affine=Dp + 4), dpp.DPP_ERR_ALIGN),
+    ({}, dict(affine=Bp + 64), dpp.DPP_ERR_ALIAS),         # affine over the sums
+    ({}, dict(stats_prev=Ep + 16), dpp.DPP_ERR_ALIAS),     # prev overlaps next
+])
+def test_groupnorm_affine_validation(kw, ptrs, want):
+    p = dict(sums=Bp, stats_prev=None, stats_next=Ep, gamma=Cp, beta=Cp + 4096, affine=Dp)
+    p.update(ptrs)
+    st = dpp.dpp_groupnorm_affine(gn(**kw), p["sums"], p["stats_prev"], p["stats_next"],
+                                  p["gamma"], p["beta"], p["affine"], stream=0,
+                                  raise_on_error=False)
+    assert st == want
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(H=9), {}, dpp.DPP_ERR_INVALID_ARG),             # the conv's own checks first
+    (dict(dtype=dpp.DPP_F32), {}, dpp.DPP_ERR_UNSUPPORTED),  # tensor-core conv only
+    ({}, dict(affine=0), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(affine_prev=0), dpp.DPP_ERR_INVALID_ARG),     # stale halo needs the old affine
+    ({}, dict(act=7), dpp.DPP_ERR_INVALID_ARG),
+    ({}, dict(G=3, sums=Ep + 65536), dpp.DPP_ERR_INVALID_ARG),  # C_out % G
+    ({}, dict(affine=Ep + 8), dpp.DPP_ERR_ALIGN),
+    ({}, dict(affine=Dp + 256), dpp.DPP_ERR_ALIAS),         # output over the affine
+    ({}, dict(sums=Dp + 512), dpp.DPP_ERR_ALIAS),           # sums inside the output
+])
+def test_conv_norm_validation(kw, ptrs, want):
+    p = dict(x=A, stale=Bp, affine=Ep, affine_prev=Ep + 4096, act=dpp.DPP_ACT_SILU, w=Cp,
+             y=Dp, G=4, sums=None)
+    p.update(ptrs)
+    st = dpp.dpp_conv3x3_norm(conv(**kw), p["x"], p["stale"], p["affine"], p["affine_prev"],
+                              p["act"], p["w"], None, p["y"], p["G"], p["sums"], stream=0,
+                              raise_on_error=False)
+    assert st == want
+
+
 def ln(**kw):
     d = dict(T=64, C=640, eps=1e-5, dtype=dpp.DPP_BF16)
     d.update(kw)

@@ -9,7 +9,9 @@ tensor-core and TMA path of the library is covered: conv (plain and with the
 GroupNorm sums), GroupNorm (two reads, and one pass on the conv's sums),
 self-attention (with its K/V state), cross-attention (one call, and the
 per-prompt K/V with the cached step), the guidance combine, the refresh, the
-linear map (plain, bias, gated GELU) and LayerNorm.
+linear map (plain, bias, gated GELU), LayerNorm, and the GroupNorm -> SiLU
+-> conv path (band sums, per-band affine, the normalising conv, the halo
+refresh).
 """
 import pytest
 import torch
@@ -86,6 +88,30 @@ def test_groupnorm_writes_inside_its_buffers(cuda_device):
     st2, y2 = Guarded((P, B, G, 2), F32, 26), Guarded((B, H, W, C), BF16, 27)
     dpp.dpp_groupnorm_apply(d, x, st_prev, sums, st2.t, gamma, beta, y2.t)
     check(st2, y2)
+
+
+def test_norm_conv_path_writes_inside_its_buffers(cuda_device):
+    # the GroupNorm -> SiLU -> conv path: band sums, per-band affine, the
+    # normalising conv (W 200 = 128 + 72, C_in 96 = 64 + 32, C_out 96 inside
+    # a 128-column tile, with its epilogue sums) and the halo refresh
+    B, H, W, Ci, Co, P, G = 2, 12, 200, 96, 96, 3, 8
+    x, stale = rnd((B, H, W, Ci), 90), rnd((B, H, W, Ci), 91)
+    gamma, beta = rnd((Ci,), 92, F32), rnd((Ci,), 93, F32)
+    gd = dpp.dpp_gn_desc(B, H, W, Ci, G, P, 1e-5, dpp.DPP_BF16, 0, 0)
+    sums = Guarded((P, B, G, 2), F64, 94)
+    dpp.dpp_groupnorm_sums(gd, x, sums.t)
+    check(sums)
+    aff, st = Guarded((P, B, Ci, 2), F32, 95), Guarded((P, B, G, 2), F32, 96)
+    dpp.dpp_groupnorm_affine(gd, sums.t, None, st.t, gamma, beta, aff.t)
+    check(aff, st, sums)
+    w = rnd((Co, 3, 3, Ci), 97, scale=0.05)
+    d = dpp.dpp_conv_desc(B, H, W, Ci, Co, P, dpp.DPP_BF16, dpp.DPP_HALO_STALE, 0)
+    y, ys = Guarded((B, H, W, Co), BF16, 98), Guarded((P, B, 32, 2), F64, 99)
+    dpp.dpp_conv3x3_norm(d, x, stale, aff.t, aff.t, dpp.DPP_ACT_SILU, w, None, y.t, 32, ys.t)
+    check(y, ys, aff)
+    halo = Guarded((B, H, W, Ci), BF16, 100)
+    dpp.dpp_refresh_halo(x, halo.t, B, H, W * Ci * 2, P)
+    check(halo)
 
 
 def test_self_attention_writes_inside_its_buffers(cuda_device):

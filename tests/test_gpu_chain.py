@@ -203,6 +203,45 @@ def chain_device_weights(wts):
     return dev
 
 
+GN_KEYS = {"gn1": ("gn1_g", "gn1_b", EPS_GN_RES), "gn2": ("gn2_g", "gn2_b", EPS_GN_RES),
+           "gn": ("gn_g", "gn_b", EPS_GN_TF)}
+
+
+def apply_affine(x64, aff, P):
+    """y = x * a + s with band p's row of the affine table [P, B, C, 2] on band
+    p's rows."""
+    a = G.f64(aff)
+    H = x64.shape[1]
+    Hp = H // P
+    y = np.empty_like(x64)
+    for p in range(P):
+        sl = slice(p * Hp, (p + 1) * Hp)
+        y[:, sl] = x64[:, sl] * a[p, :, None, None, :, 0] + a[p, :, None, None, :, 1]
+    return y
+
+
+def oracle_op_fused(name, pre, prev, norm_prev, W, ch):
+    """The fused ResNet ops: gn1/gn2 publish an affine table, so they are
+    judged by the displaced GroupNorm it applies; conv1/conv2 read the raw
+    tensor and normalise it on load, so the oracle composes SiLU(displaced
+    GroupNorm) of the op's GPU input (stale statistics from the previous
+    step's input) with the displaced conv, whose stale input is the
+    normalised tensor the oracle formed at the previous step.  Returns
+    (value to compare, normalised input for the next step or None)."""
+    P, Gr = ch.P, ch.G
+    f = lambda k: G.f64(pre[k])
+    S = lambda k: f(k) if prev is None else G.f64(prev[k])
+    g = {"gn1": "gn1", "gn2": "gn2", "conv1": "gn1", "conv2": "gn2"}[name]
+    kg, kb, eps = GN_KEYS[g]
+    gn = oracle.displaced_groupnorm(f("x"), S("x"), Gr, eps, W[kg], W[kb], P)
+    if name in ("gn1", "gn2"):
+        return gn, None
+    z = OB.silu(gn)
+    z_prev = z if norm_prev is None else norm_prev
+    y = oracle.displaced_conv3x3(z, z_prev, W[name + "_w"], W[name + "_b"], P)
+    return (y + f("out") if name == "conv2" else y), z
+
+
 def oracle_op(name, pre, post, prev, W, ch):
     """The oracle's value of one op of the chain on the GPU's own inputs
     (upcast); prev: the same op's inputs at the previous step (its stale
@@ -241,13 +280,17 @@ def oracle_op(name, pre, post, prev, W, ch):
     raise KeyError(name)
 
 
-def test_chain_two_steps_op_by_op_and_end_to_end(cuda_device):
+@pytest.mark.parametrize("fuse_norm", [True, False])
+def test_chain_two_steps_op_by_op_and_end_to_end(cuda_device, fuse_norm):
     ch = CH
     wts = wl.chain_weights(ch)
     W = {k: G.f64(v) for k, v in wts.items()}
     xs, ctx = wl.chain_inputs(ch, 1)
     chain = BlockChain(ch.B, ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx,
-                       chain_device_weights(wts), "cuda", ff_mult=ch.ff_mult)
+                       chain_device_weights(wts), "cuda", ff_mult=ch.ff_mult,
+                       fuse_norm=fuse_norm)
+    fused_ops = ("gn1", "conv1", "gn2", "conv2") if fuse_norm else ()
+    norm_prev = {}
     ctx_d = ctx.to("cuda")
     seen = {}
 
@@ -268,7 +311,16 @@ def test_chain_two_steps_op_by_op_and_end_to_end(cuda_device):
             pre, post = seen[(name, "pre")], seen[(name, "post")]
             inputs[name] = pre
             prev = None if prev_inputs is None else prev_inputs[name]
-            want = oracle_op(name, pre, post, prev, W, ch)
+            if name in ("gn1", "gn2") and fuse_norm:
+                want, _ = oracle_op_fused(name, pre, prev, None, W, ch)
+                got = apply_affine(G.f64(pre["x"]), post["out"], ch.P)
+                G.assert_rms_close(got, want, 1e-4, f"step {step} op {name} (affine)")
+                continue
+            if name in fused_ops:
+                want, norm_prev[name] = oracle_op_fused(name, pre, prev, norm_prev.get(name),
+                                                        W, ch)
+            else:
+                want = oracle_op(name, pre, post, prev, W, ch)
             got = G.f64(post["out"]).reshape(want.shape)
             check(got, want, BF16, f"step {step} op {name}")
         prev_inputs = inputs
@@ -287,14 +339,16 @@ def test_chain_two_steps_op_by_op_and_end_to_end(cuda_device):
         assert float(np.sqrt(np.mean(err ** 2))) <= 1e-2 * rms, step
 
 
-def test_chain_launches_only_library_kernels_and_repeats(cuda_device):
+@pytest.mark.parametrize("fuse_norm,launches", [(True, 24), (False, 22)])
+def test_chain_launches_only_library_kernels_and_repeats(cuda_device, fuse_norm, launches):
     # the same input twice: the displaced second step reads states equal to
     # its own fresh inputs, so it reproduces the synchronous output
     ch = CH
     wts = wl.chain_weights(ch)
     xs, ctx = wl.chain_inputs(ch, 0)
     chain = BlockChain(ch.B, ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx,
-                       chain_device_weights(wts), "cuda", ff_mult=ch.ff_mult)
+                       chain_device_weights(wts), "cuda", ff_mult=ch.ff_mult,
+                       fuse_norm=fuse_norm)
     ctx_d = ctx.to("cuda")
     outs = []
     for step in range(2):
@@ -302,12 +356,13 @@ def test_chain_launches_only_library_kernels_and_repeats(cuda_device):
         n0 = dpp.dpp_launch_count()
         chain.step(x, ctx_d)
         torch.cuda.synchronize()
-        assert dpp.dpp_launch_count() - n0 == 22
+        assert dpp.dpp_launch_count() - n0 == launches
         outs.append(G.f64(x))
     check(outs[1], outs[0], BF16, "repeated input, displaced vs synchronous step")
 
 
-def test_chain_resumes_bit_identical_from_a_checkpoint(cuda_device):
+@pytest.mark.parametrize("fuse_norm", [True, False])
+def test_chain_resumes_bit_identical_from_a_checkpoint(cuda_device, fuse_norm):
     """Checkpoint / resume of the displaced states: a chain stepped four times
     without a break, against one stepped twice, checkpointed to host memory,
     dropped, and a fresh chain (new device buffers, garbage before the load)
@@ -318,6 +373,7 @@ def test_chain_resumes_bit_identical_from_a_checkpoint(cuda_device):
     xs, ctx = wl.chain_inputs(ch, 3)
     ctx_d = ctx.to("cuda")
     args = (ch.B, ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx, wts, "cuda")
+    kw = dict(ff_mult=ch.ff_mult, fuse_norm=fuse_norm)
 
     def run(chain, steps, x):
         for s in steps:
@@ -326,17 +382,17 @@ def test_chain_resumes_bit_identical_from_a_checkpoint(cuda_device):
         torch.cuda.synchronize()
         return x
 
-    full = BlockChain(*args, ff_mult=ch.ff_mult)
+    full = BlockChain(*args, **kw)
     x_full = run(full, range(4), xs[0].to("cuda", copy=True))
-    first = BlockChain(*args, ff_mult=ch.ff_mult)
+    first = BlockChain(*args, **kw)
     x_part = run(first, range(2), xs[0].to("cuda", copy=True))
     sd = first.state_dict()
-    assert sd["k"] == 2 and all(name in sd for name in BlockChain.STATES)
+    assert sd["k"] == 2 and all(name in sd for name in first.STATES)
     x_host = x_part.cpu()
     del first, x_part
     torch.cuda.empty_cache()
-    resumed = BlockChain(*args, ff_mult=ch.ff_mult)
-    for name in BlockChain.STATES:  # the fresh chain's buffers hold garbage
+    resumed = BlockChain(*args, **kw)
+    for name in resumed.STATES:  # the fresh chain's buffers hold garbage
         for t in getattr(resumed, name):
             t.view(torch.uint8).fill_(0x7f)
     resumed.load_state_dict(sd)
@@ -345,7 +401,7 @@ def test_chain_resumes_bit_identical_from_a_checkpoint(cuda_device):
     assert torch.equal(x_res, x_full)
     got, want = resumed.state_dict(), full.state_dict()
     assert got["k"] == want["k"] == 4
-    for name in BlockChain.STATES:
+    for name in resumed.STATES:
         assert torch.equal(got[name], want[name]), name
 
 
