@@ -694,8 +694,10 @@ def time_chain(dev, steps, warmup=2):
     with displaced patch parallelism at 3840px: latent 2 x 240 x 240 x 640 in
     8 bands, 10 heads, text context 77 x 2048.  Times `steps` displaced steps
     back to back, then the same number again with an event pair around every
-    op, then the two guidance branches as chains of batch 1 run serially and
-    on two streams; returns the per-step figures."""
+    op, then the chain with the GroupNorm -> SiLU applied in the convs' loads
+    (for comparison with the default, which stores the normalised tensors),
+    then the two guidance branches as chains of batch 1 run serially and on
+    two streams; returns the per-step figures."""
     import displaced_patch_parallelism_02_b300 as dpp
     from displaced_patch_parallelism_02_b300.chain import OPS, BlockChain
     ch = wl.CHAINS["sdxl_3840_level2"]
@@ -739,6 +741,23 @@ def time_chain(dev, steps, warmup=2):
     flop = chain.flops()
     del chain
     torch.cuda.empty_cache()
+    # the same chain with the ResNet block's GroupNorm -> SiLU applied by the
+    # convs as they load their inputs (never stored), for comparison
+    fused = BlockChain(ch.B, ch.H, ch.W, ch.C, ch.heads, ch.P, ch.G, ch.n_ctx, ch.c_ctx, wts,
+                        dev, ff_mult=ch.ff_mult, fuse_norm=True)
+    xs_ = x.clone()
+    for _ in range(max(warmup, 1)):
+        fused.step(xs_, ctx, stream=s)
+    torch.cuda.synchronize(dev)
+    a.record(s)
+    for _ in range(steps):
+        fused.step(xs_, ctx, stream=s)
+    b.record(s)
+    torch.cuda.synchronize(dev)
+    ms_fused = a.elapsed_time(b) / max(steps, 1)
+    ok = ok and dpp.dpp_device_status() == dpp.DPP_OK
+    del fused, xs_
+    torch.cuda.empty_cache()
     # the guided pair as two branches of batch 1 (condition-based partition):
     # serially on one stream, and on two streams (the parallel stage)
     from displaced_patch_parallelism_02_b300.chain import BranchPair
@@ -764,6 +783,7 @@ def time_chain(dev, steps, warmup=2):
             "heads": ch.heads, "context": [ch.n_ctx, ch.c_ctx], "steps": steps,
             "ms_per_step": ms, "tflops": flop / (ms / 1e3) / 1e12, "step_flop": flop,
             "launches_per_step": launches, "ok": ok,
+            "norm_in_conv": False, "ms_per_step_norm_in_conv": ms_fused,
             "ops_ms": {n: round(v, 4) for n, v in op_ms.items()},
             "schedules_ms_per_step": {"batched": ms, **sched}}
 

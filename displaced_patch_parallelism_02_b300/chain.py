@@ -7,10 +7,10 @@ buffers); the layers DistriFusion replaces (convolutions, GroupNorms, self-
 attention) read the previous step's state of the other bands, the per-token
 layers (LayerNorm, projections, the gated feed-forward) need none:
 
-  ResNet block   h1 = conv1(SiLU(GN1(x))) + b1  dpp_groupnorm_sums + dpp_groupnorm_affine,
-                                                dpp_conv3x3_norm (sums for GN2)
-                 x += conv2(SiLU(GN2(h1))) + b2 dpp_groupnorm_affine (conv1's sums),
-                                                dpp_conv3x3_norm (accumulate; sums for GN)
+  ResNet block   g1 = SiLU(GN1(x))              dpp_groupnorm (act SiLU)
+                 h1 = conv1(g1) + b1            dpp_conv3x3_gn (sums for GN2)
+                 g2 = SiLU(GN2(h1))             dpp_groupnorm_apply (act SiLU)
+                 x += conv2(g2) + b2            dpp_conv3x3_gn (accumulate; sums for GN)
   transformer    g = GN(x)                      dpp_groupnorm_apply
                  h = g Wpi^T + bpi              dpp_linear
                  h += attn1(LN1(h))             dpp_layernorm, dpp_self_attn (accumulate)
@@ -18,11 +18,13 @@ layers (LayerNorm, projections, the gated feed-forward) need none:
                  h += GEGLU(LN3(h)) W2^T + b2   dpp_layernorm, dpp_linear (GEGLU), dpp_linear
                  x += h Wpo^T + bpo             dpp_linear (accumulate)
 
-The ResNet block's GroupNorms are reduced to a scale and shift per band,
-image and channel that the following conv applies (with the SiLU) as it loads
-its input, so the normalised tensors are never stored; with fuse_norm=False
-they are (dpp_groupnorm / dpp_groupnorm_apply with act SiLU, then
-dpp_conv3x3_gn), which gives the same results up to rounding.
+With fuse_norm=True the ResNet block's GroupNorms are instead reduced to a
+scale and shift per band, image and channel (dpp_groupnorm_sums,
+dpp_groupnorm_affine) that the following conv applies with the SiLU as it
+loads its input (dpp_conv3x3_norm), so the normalised tensors are never
+stored; the results are the same up to rounding.  On B300 the stored path is
+the faster one at the SDXL shapes (the convs are bound by shared-memory
+bandwidth, which the on-load transform adds to), so it is the default.
 
 The chain runs in place on x (the residual stream).  On one GPU every band's
 fresh activations of step t are all in HBM, so the stale state of step t+1 is
@@ -99,7 +101,7 @@ class BlockChain:
     affines); ff1_w is [2 F, C] (value rows, then gate rows), ff2_w [C, F]."""
 
     def __init__(self, B, H, W, C, heads, P, G, n_ctx, c_ctx, weights, device,
-                 ff_mult=4, eps_gn_res=1e-5, eps_gn_tf=1e-6, eps_ln=1e-5, fuse_norm=True):
+                 ff_mult=4, eps_gn_res=1e-5, eps_gn_tf=1e-6, eps_ln=1e-5, fuse_norm=False):
         self.B, self.H, self.W, self.C, self.P, self.G = B, H, W, C, P, G
         self.fuse_norm = bool(fuse_norm)
         self.heads, self.n_ctx, self.c_ctx, self.F = heads, n_ctx, c_ctx, ff_mult * C

@@ -360,7 +360,7 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 //
 // A k-step is one input row (dy) and one 64-channel block: the producer
 // loads the row's 130-pixel strip w0-1 .. w0+128 once (TMA, 128-byte
-// swizzle), four transform warps normalise it in place in shared memory,
+// swizzle), eight transform warps normalise it in place in shared memory,
 // and the three horizontal taps are the strip read from row 0, 1 and 2:
 // the MMA's A descriptor starts dx * 128 bytes into the strip (the swizzle
 // follows the absolute shared-memory address, so a row-offset start reads
@@ -373,14 +373,15 @@ conv_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 //   warp 6      weight producer (B ring, SB slots of 3 taps)
 //   warp 1      TMEM owner and MMA issuer: per k-step 3 taps x 4 K-steps
 //   warps 2..5  epilogue (as conv_tc_kernel)
-//   warps 7..10 transform: thread t normalises 16-byte chunk t % 8 of
-//               pixels t / 8 + 16 i of the strip (conflict-free: 4 whole
-//               128-byte rows per warp access)
+//   warps 7..14 transform: thread t normalises 16-byte chunk t % 8 of
+//               pixels t / 8 + 32 i of the strip (conflict-free: 4 whole
+//               128-byte rows per warp access); two warps per scheduler
+//               hide each other's load and special-function latency
 // The activation is SiLU(v) = h + h tanh(h), h = v / 2 (PTX tanh.approx.f32:
 // one special-function op per value, |error| about |h| 2^-11), so the
 // transform's special-function work stays inside the tensor time of a
 // k-step.
-constexpr int kNormThreads = 352;
+constexpr int kNormThreads = 480;
 constexpr uint32_t kStripRows = BM + 2;
 constexpr uint32_t kStripBytes = kStripRows * 128;                  // transaction bytes
 constexpr uint32_t kStripSlot = (kStripBytes + 1023u) & ~1023u;     // 1024-aligned slots
@@ -429,7 +430,7 @@ conv_norm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&a_ready[s], 4);
+      mbar_init(&a_ready[s], 8);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < SB; ++s) {
@@ -569,7 +570,7 @@ conv_norm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
       mbar_drain(drain, 0);
     }
   } else if (warp >= 7) {  // ---------------------------------- transform
-    const int tid = threadIdx.x - 7 * 32;
+    const int tid = threadIdx.x - 7 * 32;  // 0 .. 255
     const int j = tid & 7, p0 = tid >> 3;
     int slot = 0;
     uint32_t phase = 0;
@@ -605,9 +606,9 @@ conv_norm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
               sh[2 * e + 1] = v.w;
             }
             uint8_t *strip = sA + slot * kStripSlot;
-#pragma unroll 3
-            for (int i = 0; i < 9; ++i) {
-              const int px = p0 + 16 * i;
+#pragma unroll
+            for (int i = 0; i < 5; ++i) {
+              const int px = p0 + 32 * i;
               const int ww = w0 - 1 + px;
               if (px < (int)kStripRows && ww >= 0 && ww < p.W) {
                 uint4 *ptr = reinterpret_cast<uint4 *>(strip + px * 128 + ((j ^ (px & 7)) << 4));

@@ -33,8 +33,9 @@ import json
 
 import torch
 
-from . import (DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_attn_desc, dpp_cfg_combine,
-               dpp_cfg_workspace_bytes, dpp_conv3x3_gn, dpp_conv_desc,
+from . import (DPP_ACT_SILU, DPP_BF16, DPP_EPI_GEGLU, DPP_EPI_NONE, dpp_attn_desc,
+               dpp_cfg_combine, dpp_cfg_workspace_bytes, dpp_conv3x3, dpp_conv3x3_gn,
+               dpp_conv3x3_norm, dpp_conv_desc,
                dpp_cross_attn_cached, dpp_cross_attn_cached_workspace_bytes, dpp_cross_attn_kv,
                dpp_device_status, dpp_gn_desc, dpp_groupnorm, dpp_groupnorm_apply,
                dpp_groupnorm_workspace_bytes, dpp_layernorm, dpp_linear, dpp_linear_desc,
@@ -84,6 +85,19 @@ def setup(args, gen):
             dpp_conv3x3_gn(cd, x, stale, w, None, y, G, sums)
             dpp_groupnorm_apply(gd, y, st_prev, sums, st_next, gamma, beta, y2)
         return call, 2.0 * B * H * W * C * 9 * C, "TFLOP/s"
+    if args.op in ("conv", "normconv"):  # displaced conv; normconv: GroupNorm + SiLU on load
+        B, H, W, C, P = args.B, args.H, args.W, args.C, args.P
+        x = _randn((B, H, W, C), gen)
+        stale = _randn((B, H, W, C), gen)
+        w = _randn((C, 3, 3, C), gen, (9 * C) ** -0.5)
+        y = torch.empty_like(x)
+        cd = dpp_conv_desc(B, H, W, C, C, P, DPP_BF16, 0, 0)
+        if args.op == "conv":
+            return (lambda: dpp_conv3x3(cd, x, stale, w, None, y)), 2.0 * B * H * W * C * 9 * C, \
+                "TFLOP/s"
+        aff = [torch.rand((P, B, C, 2), generator=gen, device="cuda") for _ in range(2)]
+        return (lambda: dpp_conv3x3_norm(cd, x, stale, aff[0], aff[1], DPP_ACT_SILU, w, None, y)), \
+            2.0 * B * H * W * C * 9 * C, "TFLOP/s"
     if args.op == "layernorm":
         T, C = args.T, args.C
         x = _randn((T, C), gen)
@@ -152,8 +166,8 @@ def setup(args, gen):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("op", choices=["linear", "cfg", "conv_gn", "layernorm", "attn", "groupnorm",
-                                   "cross"])
+    ap.add_argument("op", choices=["linear", "cfg", "conv", "normconv", "conv_gn", "layernorm",
+                                   "attn", "groupnorm", "cross"])
     ap.add_argument("--M", type=int, default=115200)
     ap.add_argument("--K", type=int, default=640)
     ap.add_argument("--N", type=int, default=640)
