@@ -25,6 +25,10 @@
 //               STATS also the per-group sums of the stored values (for a
 //               GroupNorm of this output), reduced over the warp's 32 pixels
 //               and added into fp64 totals per (band, image, group).
+//
+// conv_norm_tc_kernel (further down) is the same conv reading its input
+// through a GroupNorm affine and SiLU applied as the input is loaded
+// (dpp_conv3x3_norm), with its K loop organised around input-row strips.
 #include "tc_common.cuh"
 
 namespace dpp {
